@@ -83,27 +83,33 @@ def torch_dtype(name: str) -> torch.dtype:
     return {"f16": torch.float16, "bf16": torch.bfloat16}[name]
 
 
-def make_qkv(w: Workload, *, seed: int | None = None, device: str = "cpu"):
+def make_qkv(w: Workload, *, seed: int | None = None, device: str = "cpu",
+             generate_on_device: bool = False):
     """Q, K, V for workload ``w`` (dense values, in the workload dtype), generated on the CPU from
     the seed and then moved to ``device``.  For q4_0 workloads K and V are the values that get
     quantized."""
     return make_tensors(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.dtype,
                         seed=w.seed if seed is None else seed, ramp=w.ramp, scale=w.scale,
-                        device=device)
+                        device=device, generate_on_device=generate_on_device)
 
 
 def make_tensors(B, Hq, Hkv, Sq, Sk, D, dtype="f16", *, seed=0, ramp=False, scale=None,
-                 device="cpu"):
-    g = torch.Generator(device="cpu").manual_seed(int(seed))
+                 device="cpu", generate_on_device=False):
+    """Q, K, V drawn from one seeded generator in Q, K, V order.  By default the draw happens on
+    the CPU (the stream the parity tests and the oracle share) and the tensors are then moved to
+    ``device``; with ``generate_on_device`` a CUDA generator with the same seed draws them in
+    place (same distribution, different stream; used for large benchmark inputs)."""
+    gdev = device if generate_on_device else "cpu"
+    g = torch.Generator(device=gdev).manual_seed(int(seed))
     dt = torch_dtype(dtype)
-    q = torch.randn(B, Hq, Sq, D, generator=g, dtype=torch.float32).to(dt)
-    k = torch.randn(B, Hkv, Sk, D, generator=g, dtype=torch.float32).to(dt)
-    v = torch.randn(B, Hkv, Sk, D, generator=g, dtype=torch.float32).to(dt)
+    q = torch.randn(B, Hq, Sq, D, generator=g, dtype=torch.float32, device=gdev).to(dt)
+    k = torch.randn(B, Hkv, Sk, D, generator=g, dtype=torch.float32, device=gdev).to(dt)
+    v = torch.randn(B, Hkv, Sk, D, generator=g, dtype=torch.float32, device=gdev).to(dt)
     if ramp:
         if scale is None:
             scale = 1.0 / math.sqrt(D)
         q[..., 0] = 8.0
-        j = torch.arange(Sk, dtype=torch.float64)
+        j = torch.arange(Sk, dtype=torch.float64, device=gdev)
         col = (2.0 * torch.floor(j / 128.0) / (8.0 * scale)).to(dt)
         k[..., 0] = col
     if device != "cpu":

@@ -1,0 +1,128 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused causal GQA flash-attention forward with an optional
+ * q4_0 K/V cache.
+ *
+ * Operation (fa_fwd): for every batch b, query head h and query row i
+ *
+ *     O[b,h,i,:] = sum_j softmax_j( scale * <Q[b,h,i,:], K[b,g,j,:]> + mask(i,j) ) * V[b,g,j,:]
+ *
+ * with g = h / (Hq / Hkv) (grouped-query heads in contiguous groups) and, when causal, key j
+ * hidden from row i iff j > q_pos_offset + i.  This is the fused prefill call of
+ * "perf(rocm): defer SDPA accumulator rescale, stage Q once per block (#2306)" (Conversation:
+ * chunked-prefill query chunks against 2K-16K keys, GQA 32/8, head dim 128; What changed: the
+ * deferred O/l rescale with its 10-point margin and Q staged once per block) and the
+ * flash_attn_func / scaled_dot_product_attention(is_causal=True) call of "Build FlashAttention
+ * (CK backend) on gfx90a" (Verification).  With kv_format = FA_KV_Q4_0 the K and V caches are
+ * q4_0 and are dequantized inside the kernel, the fused V dequant that "FlashAttention on gfx90a:
+ * Why It's Broken and How to Fix It" (Why FA-off Can't Do V Quantization; The V Dequantization
+ * Gap) describes as what the flash-attention path provides.
+ *
+ * Conventions shared by every entry point
+ *  - All tensors are device memory owned by the caller, contiguous, head-major:
+ *      Q, O : [B, Hq, Sq, D]        K, V (dense) : [B, Hkv, Sk, D]   (dtype of Q)
+ *    Every pointer must be 16-byte aligned.
+ *  - q4_0 tensor (one buffer per K or V, built by fa_quantize_q4_0), for a [B, H, S, D] source:
+ *      nibble plane [B, H, S, D/2] uint8 at offset 0: byte j of each 32-element block holds
+ *        element j in its low nibble and element j+16 in its high nibble;
+ *      scale plane  [B, H, S, D/32] fp16 at offset fa_q4_0_scale_offset(B,H,S,D) (256-aligned).
+ *    Element value = (nibble - 8) * scale.  The pages name q4_0 (-ctk q4_0 -ctv q4_0) without
+ *    fixing its bits; this planar layout carries exactly the bits of the usual 18-byte
+ *    {fp16 d, 16 bytes of nibbles} block and converts to it losslessly.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream).  The return value
+ *    reports host-side argument checks and launch errors only; faults detected on the device
+ *    (a bounded wait that ran out) are reported by fa_get_status.
+ *  - Calls are thread-safe; concurrent calls on different streams are independent.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape, bad causal offset, scale */
+  FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented: D not in {64, 128}, group size > 8 */
+  FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  FA_ERR_TIMEOUT = 4        /* a device-side bounded wait ran out (see fa_get_status) */
+} fa_status;
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+typedef enum {
+  FA_KV_DENSE = 0, /* K, V in the dtype of Q */
+  FA_KV_Q4_0 = 1   /* K, V are q4_0 tensors (see above) */
+} fa_kv_format;
+
+/* Attention forward.
+ *  q, o      : [B, Hq, Sq, D] in `dtype`
+ *  k, v      : [B, Hkv, Sk, D] in `dtype` (FA_KV_DENSE) or q4_0 tensors of that shape
+ *  B, Hq, Hkv, Sq, Sk >= 1, Hq % Hkv == 0, Hq / Hkv <= 8 when Sq == 1; D in {64, 128}
+ *  q_pos_offset : absolute position of query row 0 (used when causal); requires
+ *                 0 <= q_pos_offset and q_pos_offset + Sq <= Sk, so that no row is fully masked
+ *                 (Sk - Sq gives the bottom-right aligned chunked-prefill mask)
+ *  causal    : nonzero for the causal mask
+ *  scale     : softmax scale, finite and > 0 (typically 1/sqrt(D))
+ * Sq == 1 runs the split-K decode kernels and needs a scratch buffer of fa_workspace_bytes();
+ * fa_fwd takes it from the stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on `stream`);
+ * use fa_fwd_ex to pass one instead.  Sq >= 2 runs the prefill kernel and needs no scratch. */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                 int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
+                 fa_dtype dtype, fa_kv_format kv_format, fa_stream_t stream);
+
+/* fa_fwd with caller-provided scratch and an optional rescale counter.
+ *  workspace, workspace_bytes : device buffer of at least fa_workspace_bytes(...) bytes (may be
+ *                 NULL when that is 0); owned by the caller, must not be used by another call in
+ *                 flight at the same time.
+ *  rescale_count : optional device int32 [B, Hq, Sq] (NULL to skip).  The prefill kernel writes
+ *                 for every query row how many times its softmax frame was moved (the first
+ *                 key block always sets it, so every value is >= 1); the deferred rescale of
+ *                 #2306 fires only on the moves after the first.  Not written when Sq == 1. */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                    int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
+                    fa_dtype dtype, fa_kv_format kv_format, void* workspace,
+                    size_t workspace_bytes, int32_t* rescale_count, fa_stream_t stream);
+
+/* Scratch bytes fa_fwd_ex needs for this shape (0 for Sq >= 2). */
+size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
+                          int causal);
+
+/* Size in bytes of a q4_0 tensor for a [B, H, S, D] source, and the offset of its scale plane. */
+size_t fa_q4_0_bytes(int B, int H, int S, int D);
+size_t fa_q4_0_scale_offset(int B, int H, int S, int D);
+
+/* Build a q4_0 tensor from x [B, H, S, D] (`dtype`).  out_q4 has fa_q4_0_bytes(B,H,S,D) bytes.
+ * The result is bit-identical to the block definition (f32 multiply and add, each rounded to
+ * nearest even; fp16 scale rounded to nearest even).  x must be finite.  D % 32 == 0. */
+fa_status fa_quantize_q4_0(const void* x, void* out_q4, int B, int H, int S, int D,
+                           fa_dtype dtype, fa_stream_t stream);
+
+/* Synchronize `stream`, then report (and clear) any device-side error recorded by this
+ * library's kernels since the last call: FA_ERR_TIMEOUT when a bounded wait inside a kernel ran
+ * out (the kernel then abandoned its work and returned), FA_ERR_CUDA when the stream reports a
+ * CUDA error, FA_OK otherwise. */
+fa_status fa_get_status(fa_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* fa_status_string(fa_status s);
+
+/* Self-test of the bounded-wait machinery: launches one tiny kernel that waits on a barrier
+ * nothing will complete, with a limit of `limit_ns` nanoseconds (clamped to [1e3, 1e9]).  The
+ * kernel records FA_ERR_TIMEOUT and returns; fa_get_status then reports it.  No GPU fault, trap
+ * or hang is involved. */
+fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

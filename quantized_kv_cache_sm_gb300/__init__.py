@@ -1,0 +1,244 @@
+"""Python binding of libfa_gb300.so: the fused causal GQA flash-attention forward for sm_103a,
+with an optional q4_0 K/V cache.
+
+Argument marshalling only: each function here turns torch tensors into the pointers, sizes and
+stream handle of the C entry point of the same name (declared in ``include/fa.h``) and raises
+``FaError`` on a non-OK status.  Every step of the computation runs in the CUDA kernels; there is
+no CPU path.  The library must have been built (``build.build()`` or ``__graft_entry__.build()``);
+if it is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_F16, FA_BF16 = 0, 1
+FA_KV_DENSE, FA_KV_Q4_0 = 0, 1
+
+EXPORTED = (
+    "fa_fwd", "fa_fwd_ex", "fa_workspace_bytes", "fa_q4_0_bytes", "fa_q4_0_scale_offset",
+    "fa_quantize_q4_0", "fa_get_status", "fa_status_string", "fa_debug_wait_timeout",
+    "fa_version",
+)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_name(status)}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library once per process (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_from(path or _build.LIB_PATH)
+        return _lib
+
+
+def load_from(p: str) -> ctypes.CDLL:
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it first (quantized_kv_cache_sm_gb300.build)")
+    lib = ctypes.CDLL(p)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fwd = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, i]
+    lib.fa_fwd.argtypes = fwd + [vp]
+    lib.fa_fwd.restype = i
+    lib.fa_fwd_ex.argtypes = fwd + [vp, sz, vp, vp]
+    lib.fa_fwd_ex.restype = i
+    lib.fa_workspace_bytes.argtypes = [i] * 8
+    lib.fa_workspace_bytes.restype = sz
+    lib.fa_q4_0_bytes.argtypes = [i] * 4
+    lib.fa_q4_0_bytes.restype = sz
+    lib.fa_q4_0_scale_offset.argtypes = [i] * 4
+    lib.fa_q4_0_scale_offset.restype = sz
+    lib.fa_quantize_q4_0.argtypes = [vp, vp, i, i, i, i, i, vp]
+    lib.fa_quantize_q4_0.restype = i
+    lib.fa_get_status.argtypes = [vp]
+    lib.fa_get_status.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_debug_wait_timeout.argtypes = [ctypes.c_int64, vp]
+    lib.fa_debug_wait_timeout.restype = i
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = i
+    return lib
+
+
+def status_name(s: int) -> str:
+    names = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
+             4: "FA_ERR_TIMEOUT"}
+    return names.get(int(s), f"status {int(s)}")
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        raise FaError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float16:
+        return FA_F16
+    if t == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {t}: use float16 or bfloat16")
+
+
+@dataclasses.dataclass
+class Q4Tensor:
+    """A q4_0 tensor of logical shape [B, H, S, D]: one uint8 device buffer holding the nibble
+    plane [B, H, S, D/2] and, at a 256-byte aligned offset, the fp16 scale plane [B, H, S, D/32]."""
+    buf: torch.Tensor
+    B: int
+    H: int
+    S: int
+    D: int
+
+    @property
+    def shape(self):
+        return (self.B, self.H, self.S, self.D)
+
+    def nibbles(self) -> torch.Tensor:
+        n = self.B * self.H * self.S * self.D // 2
+        return self.buf[:n].view(self.B, self.H, self.S, self.D // 2)
+
+    def scales(self) -> torch.Tensor:
+        off = fa_q4_0_scale_offset(self.B, self.H, self.S, self.D)
+        n = self.B * self.H * self.S * (self.D // 32) * 2
+        return self.buf[off:off + n].view(torch.float16).view(self.B, self.H, self.S, self.D // 32)
+
+    def data_ptr(self) -> int:
+        return self.buf.data_ptr()
+
+
+def _kv_args(k, v):
+    if isinstance(k, Q4Tensor) != isinstance(v, Q4Tensor):
+        raise TypeError("k and v must both be dense tensors or both be Q4Tensor")
+    if isinstance(k, Q4Tensor):
+        if k.shape != v.shape:
+            raise ValueError("k and v shapes differ")
+        return FA_KV_Q4_0, k.shape
+    if k.shape != v.shape or k.dim() != 4:
+        raise ValueError("k and v must both be [B, Hkv, Sk, D]")
+    if not (k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("k and v must be contiguous")
+    return FA_KV_DENSE, tuple(k.shape)
+
+
+def _fwd_args(q, k, v, o, causal, q_pos_offset, scale):
+    if q.dim() != 4 or not q.is_contiguous() or not o.is_contiguous() or o.shape != q.shape:
+        raise ValueError("q and o must be contiguous [B, Hq, Sq, D] tensors of the same shape")
+    if o.dtype != q.dtype:
+        raise TypeError("o must have the dtype of q")
+    kv_format, (Bk, Hkv, Sk, Dk) = _kv_args(k, v)
+    B, Hq, Sq, D = q.shape
+    if Bk != B or Dk != D:
+        raise ValueError("k/v batch or head dim does not match q")
+    if kv_format == FA_KV_DENSE and k.dtype != q.dtype:
+        raise TypeError("dense k/v must have the dtype of q")
+    if scale is None:
+        scale = D ** -0.5
+    if q_pos_offset is None:
+        q_pos_offset = Sk - Sq
+    return (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Sk, D,
+            int(q_pos_offset), int(bool(causal)), float(scale), _dtype_code(q.dtype), kv_format)
+
+
+def fa_fwd(q, k, v, o=None, *, causal: bool = True, q_pos_offset: int | None = None,
+           scale: float | None = None, stream=None) -> torch.Tensor:
+    """O = softmax(scale Q K^T + causal mask) V.  q [B,Hq,Sq,D]; k, v [B,Hkv,Sk,D] dense (dtype of
+    q) or Q4Tensor.  q_pos_offset defaults to Sk - Sq (bottom-right aligned chunk), scale to
+    1/sqrt(D).  Returns o (allocated when not given)."""
+    if o is None:
+        o = torch.empty_like(q)
+    lib = load()
+    args = _fwd_args(q, k, v, o, causal, q_pos_offset, scale)
+    _check(lib.fa_fwd(*args, _stream(stream)), "fa_fwd")
+    return o
+
+
+def fa_fwd_ex(q, k, v, o=None, *, causal: bool = True, q_pos_offset: int | None = None,
+              scale: float | None = None, workspace: torch.Tensor | None = None,
+              rescale_count: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fa_fwd with caller-provided scratch (uint8 device tensor of at least fa_workspace_bytes)
+    and an optional int32 [B, Hq, Sq] rescale counter."""
+    if o is None:
+        o = torch.empty_like(q)
+    lib = load()
+    args = _fwd_args(q, k, v, o, causal, q_pos_offset, scale)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc_ptr = None
+    if rescale_count is not None:
+        if rescale_count.dtype != torch.int32 or rescale_count.numel() != q.shape[0] * q.shape[1] * q.shape[2]:
+            raise ValueError("rescale_count must be int32 [B, Hq, Sq]")
+        rc_ptr = rescale_count.data_ptr()
+    _check(lib.fa_fwd_ex(*args, ws_ptr, ws_bytes, rc_ptr, _stream(stream)), "fa_fwd_ex")
+    return o
+
+
+def fa_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal) -> int:
+    return int(load().fa_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, int(bool(causal))))
+
+
+def fa_q4_0_bytes(B, H, S, D) -> int:
+    return int(load().fa_q4_0_bytes(B, H, S, D))
+
+
+def fa_q4_0_scale_offset(B, H, S, D) -> int:
+    return int(load().fa_q4_0_scale_offset(B, H, S, D))
+
+
+def fa_quantize_q4_0(x: torch.Tensor, out: Q4Tensor | None = None, *, stream=None) -> Q4Tensor:
+    """Build the q4_0 tensor of x [B, H, S, D] (float16/bfloat16, D % 32 == 0)."""
+    if x.dim() != 4 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [B, H, S, D] tensor")
+    B, H, S, D = x.shape
+    lib = load()
+    if out is None:
+        nbytes = fa_q4_0_bytes(B, H, S, D)
+        if nbytes == 0:
+            raise ValueError("D must be a positive multiple of 32")
+        out = Q4Tensor(torch.empty(nbytes, dtype=torch.uint8, device=x.device), B, H, S, D)
+    _check(lib.fa_quantize_q4_0(x.data_ptr(), out.data_ptr(), B, H, S, D, _dtype_code(x.dtype),
+                                _stream(stream)), "fa_quantize_q4_0")
+    return out
+
+
+def fa_get_status(stream=None) -> int:
+    return int(load().fa_get_status(_stream(stream)))
+
+
+def fa_status_string(s: int) -> str:
+    return load().fa_status_string(int(s)).decode()
+
+
+def fa_debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load().fa_debug_wait_timeout(int(limit_ns), _stream(stream)), "fa_debug_wait_timeout")
+
+
+def fa_version() -> int:
+    return int(load().fa_version())

@@ -1,0 +1,289 @@
+// C-ABI front end: argument checks, TMA descriptors, kernel dispatch, device status.
+#include <math.h>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+__device__ uint32_t g_debug_error;
+
+namespace {
+
+__global__ void debug_wait_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing arrives on this barrier: the bounded wait must give up and record the timeout
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, &g_debug_error, limit_ns);
+    mbar_arrive(smem_u32(&bar));  // leave the barrier completed
+  }
+  __syncthreads();
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D tiled map over a contiguous [d2][d1][d0] tensor; box = {box0, box1, 1}.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t d0,
+              uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+size_t q4_scale_offset(int64_t rows, int D) {
+  const size_t nib = static_cast<size_t>(rows) * (D / 2);
+  return (nib + 255) / 256 * 256;
+}
+
+fa_status check_common(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
+                       int causal, float scale, int dtype, int kv_format) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || Hkv > 65535 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (kv_format != FA_KV_DENSE && kv_format != FA_KV_Q4_0) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (causal && (q_pos_offset < 0 || static_cast<int64_t>(q_pos_offset) + Sq > Sk))
+    return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if ((Sq + 127) / 128 > 65535) return FA_ERR_UNSUPPORTED;
+  if (Sq == 1 && Hq / Hkv > 8) return FA_ERR_UNSUPPORTED;
+  // offsets are 64-bit; keep every tensor far below the address-space limits
+  if (static_cast<int64_t>(B) * Hq * Sq * D >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Hkv * Sk * D >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t workspace_for(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
+                     int causal, int* nsplit_out, int* chunk_out) {
+  if (Sq != 1) return 0;
+  const int sk_eff = causal ? q_pos_offset + 1 : Sk;
+  int ns = 1, ck = sk_eff;
+  decode_plan(B, Hkv, sk_eff, num_sms(), &ns, &ck);
+  if (nsplit_out) *nsplit_out = ns;
+  if (chunk_out) *chunk_out = ck;
+  return static_cast<size_t>(B) * Hq * ns * (D + 4) * sizeof(float);
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+size_t fa_q4_0_scale_offset(int B, int H, int S, int D) {
+  if (B < 1 || H < 1 || S < 1 || D < 32 || D % 32) return 0;
+  return q4_scale_offset(static_cast<int64_t>(B) * H * S, D);
+}
+
+size_t fa_q4_0_bytes(int B, int H, int S, int D) {
+  if (B < 1 || H < 1 || S < 1 || D < 32 || D % 32) return 0;
+  const int64_t rows = static_cast<int64_t>(B) * H * S;
+  return q4_scale_offset(rows, D) + static_cast<size_t>(rows) * (D / 32) * 2;
+}
+
+size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
+                          int causal) {
+  if (check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, 1.f, FA_F16, FA_KV_DENSE) !=
+      FA_OK)
+    return 0;
+  return workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, nullptr, nullptr);
+}
+
+fa_status fa_quantize_q4_0(const void* x, void* out_q4, int B, int H, int S, int D,
+                           fa_dtype dtype, fa_stream_t stream) {
+  if (!aligned16(x) || !aligned16(out_q4)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || D < 32 || D % 32) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(B) * H * S;
+  uint8_t* base = static_cast<uint8_t*>(out_q4);
+  const cudaError_t e = quantize_launch(x, base, base + q4_scale_offset(rows, D), rows, D,
+                                        dtype == FA_BF16, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                    int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
+                    fa_dtype dtype, fa_kv_format kv_format, void* workspace,
+                    size_t workspace_bytes, int32_t* rescale_count, fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  const fa_status st =
+      check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale, dtype, kv_format);
+  if (st != FA_OK) return st;
+  const bool bf16 = dtype == FA_BF16;
+  const bool q4 = kv_format == FA_KV_Q4_0;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const CUtensorMapDataType tdt =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t BHkv = static_cast<uint64_t>(B) * Hkv;
+  const size_t kv_scale_off = q4 ? q4_scale_offset(static_cast<int64_t>(BHkv) * Sk, D) : 0;
+  const CUtensorMapSwizzle nib_sw =
+      D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+
+  if (Sq == 1) {
+    int nsplit = 1, chunk = 1;
+    const size_t need =
+        workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, &nsplit, &chunk);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+      return FA_ERR_INVALID_ARG;
+    DecodeLaunch L;
+    bool ok;
+    if (q4) {
+      ok = make_map(&L.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, 64,
+                    nib_sw) &&
+           make_map(&L.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, 64,
+                    nib_sw);
+      L.k_scale = static_cast<const uint8_t*>(k) + kv_scale_off;
+      L.v_scale = static_cast<const uint8_t*>(v) + kv_scale_off;
+    } else {
+      ok = make_map(&L.tm_k, k, tdt, 2, D, Sk, BHkv, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&L.tm_v, v, tdt, 2, D, Sk, BHkv, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+      L.k_scale = L.v_scale = nullptr;
+    }
+    if (!ok) return FA_ERR_CUDA;
+    L.q = q;
+    L.o = o;
+    L.partial = static_cast<float*>(workspace);
+    L.B = B;
+    L.Hq = Hq;
+    L.Hkv = Hkv;
+    L.Sk = Sk;
+    L.Sk_eff = causal ? q_pos_offset + 1 : Sk;
+    L.D = D;
+    L.nsplit = nsplit;
+    L.chunk = chunk;
+    L.scale = scale;
+    L.bf16 = bf16;
+    L.q4 = q4;
+    return decode_launch(L, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  PrefillLaunch L;
+  bool ok = make_map(&L.tm_q, q, tdt, 2, D, Sq, static_cast<uint64_t>(B) * Hq, 64, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (q4) {
+    ok = ok &&
+         make_map(&L.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, 128,
+                  nib_sw) &&
+         make_map(&L.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, 128,
+                  nib_sw);
+    L.k_scale = static_cast<const uint8_t*>(k) + kv_scale_off;
+    L.v_scale = static_cast<const uint8_t*>(v) + kv_scale_off;
+  } else {
+    ok = ok && make_map(&L.tm_k, k, tdt, 2, D, Sk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&L.tm_v, v, tdt, 2, D, Sk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    L.k_scale = L.v_scale = nullptr;
+  }
+  if (!ok) return FA_ERR_CUDA;
+  L.o = o;
+  L.rescale_count = rescale_count;
+  L.B = B;
+  L.Hq = Hq;
+  L.Hkv = Hkv;
+  L.Sq = Sq;
+  L.Sk = Sk;
+  L.D = D;
+  L.q_pos_offset = causal ? q_pos_offset : 0;
+  L.causal = causal ? 1 : 0;
+  L.scale = scale;
+  L.bf16 = bf16;
+  L.q4 = q4;
+  return prefill_launch(L, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                 int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
+                 fa_dtype dtype, fa_kv_format kv_format, fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  const fa_status st =
+      check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale, dtype, kv_format);
+  if (st != FA_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t need = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, nullptr,
+                                    nullptr);
+  void* ws = nullptr;
+  if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess) return FA_ERR_CUDA;
+  const fa_status r = fa_fwd_ex(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale,
+                                dtype, kv_format, ws, need, nullptr, stream);
+  if (ws && cudaFreeAsync(ws, s) != cudaSuccess && r == FA_OK) return FA_ERR_CUDA;
+  return r;
+}
+
+fa_status fa_get_status(fa_stream_t stream) {
+  const cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  const uint32_t a = prefill_take_error();
+  const uint32_t b = decode_take_error();
+  uint32_t c = 0;
+  if (cudaMemcpyFromSymbol(&c, g_debug_error, sizeof(c)) != cudaSuccess) return FA_ERR_CUDA;
+  const uint32_t z = 0;
+  if (c != 0 && cudaMemcpyToSymbol(g_debug_error, &z, sizeof(z)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (a == 0xffffffffu || b == 0xffffffffu) return FA_ERR_CUDA;
+  if (a || b || c) return FA_ERR_TIMEOUT;
+  return FA_OK;
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream) {
+  if (limit_ns < 1000) limit_ns = 1000;
+  if (limit_ns > 1000000000) limit_ns = 1000000000;
+  debug_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint64_t>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+// Internal host-side interfaces between the C-ABI front end (fa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+struct PrefillLaunch {
+  CUtensorMap tm_q, tm_k, tm_v;  // dense: Q/K/V tiles; q4_0: Q tiles and K/V nibble tiles
+  void* o;
+  const void* k_scale;           // q4_0 only
+  const void* v_scale;
+  int32_t* rescale_count;
+  int B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal;
+  float scale;
+  bool bf16, q4;
+};
+cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream);
+uint32_t prefill_take_error();
+
+struct DecodeLaunch {
+  CUtensorMap tm_k, tm_v;        // K/V tiles (dense) or nibble tiles (q4_0)
+  const void* q;
+  void* o;
+  const void* k_scale;           // q4_0 only
+  const void* v_scale;
+  float* partial;                // [B, Hkv, nsplit, G, D + 2] f32 (workspace)
+  int B, Hq, Hkv, Sk_eff, Sk, D, nsplit, chunk;
+  float scale;
+  bool bf16, q4;
+};
+cudaError_t decode_launch(const DecodeLaunch& L, cudaStream_t stream);
+uint32_t decode_take_error();
+// decode work split for a given shape (shared by the workspace query and the launch)
+void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, int* nsplit, int* chunk);
+
+cudaError_t quantize_launch(const void* x, void* nib, void* scale, int64_t rows, int D, bool bf16,
+                            cudaStream_t stream);
+
+cudaError_t debug_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
+uint32_t debug_take_error();
+
+}  // namespace fa

@@ -1,0 +1,576 @@
+// Fused causal GQA flash-attention forward (chunked prefill) for sm_103a.
+//
+// What it computes: O = softmax(scale * Q K^T + causal mask) V per query head, with query head h
+// reading key/value head h / (Hq / Hkv), and the query chunk placed at absolute positions
+// q_pos_offset .. q_pos_offset + Sq - 1 (a key is visible when its position is <= the row's).
+// This is the fused kernel of "perf(rocm): defer SDPA accumulator rescale, stage Q once per
+// block (#2306)" (Conversation; What changed), rebuilt for tcgen05:
+//
+//  * one CTA owns 128 query rows of one query head; Q is brought into shared memory once by TMA
+//    and stays there for the CTA's whole key range ("Q is staged once per block");
+//  * K and V tiles of 128 keys stream through a ring of shared-memory stages, either by TMA
+//    (dense f16/bf16 cache) or as q4_0 nibble/scale tiles that dequant warps expand into the same
+//    f16/bf16 swizzled layout (the fused K and V dequant of "FlashAttention on gfx90a: Why It's
+//    Broken and How to Fix It", Why FA-off Can't Do V Quantization, point 5);
+//  * S = Q K^T and O += P V are tcgen05.mma into tensor memory (S double-buffered, O resident);
+//  * the softmax warps own one row each: block max, the deferred rescale, P = 2^(t - f) written
+//    back over S as f16/bf16 for the PV MMA, running row sum l;
+//  * deferred rescale (#2306, kFaWmmaRescaleMargin): a row keeps its frame f until a block max
+//    exceeds f by more than 10 natural-log units; only then are O and l multiplied by
+//    e^(f_old - f_new).  P stays below e^10 = 22026 in every frame.
+//
+// Warp roles (dense: 6 warps; q4_0: 10 warps):
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM allocator + MMA issuer (one lane)
+//   warps 2..5  softmax / rescale / epilogue, one query row per thread
+//   warps 6..9  q4_0 dequant (q4_0 variant only), one key row per thread
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+__device__ uint32_t g_prefill_error;
+
+namespace {
+
+constexpr int kBM = 128;                      // query rows per CTA
+constexpr int kBN = 128;                      // keys per tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMarginLog2 = 10.0f * kLog2e; // the 10-point margin, in base-2 units
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+
+template <int D, bool Q4>
+struct Cfg {
+  static constexpr int kTileBytes = kBN * D * 2;          // one f16/bf16 K or V tile
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kStages = Q4 ? 3 : (D == 128 ? 4 : 7);
+  static constexpr int kRawStages = Q4 ? 4 : 0;
+  static constexpr int kNibRow = D / 2;                   // bytes of nibbles per key
+  static constexpr int kScaleRow = D / 32 * 2;            // bytes of scales per key
+  static constexpr int kRawNib = kBN * kNibRow;
+  static constexpr int kRawBytes = ((kRawNib + kBN * kScaleRow) + 1023) / 1024 * 1024;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffRing = kOffQ + kQBytes;
+  static constexpr int kOffRaw = kOffRing + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  static constexpr int kWarps = Q4 ? 10 : 6;
+  static constexpr int kThreads = kWarps * 32;
+};
+
+// barrier slots (8 bytes each) inside the barrier area
+enum {
+  kBarQFull = 0,
+  kBarSFull0 = 1,
+  kBarSFull1 = 2,
+  kBarPReady0 = 3,
+  kBarPReady1 = 4,
+  kBarODone = 5,
+  kBarDrain = 6,
+  kBarRingFull = 8,    // + stage   (up to 8 stages)
+  kBarRingEmpty = 16,  // + stage
+  kBarRawFull = 24,    // + raw stage
+  kBarRawEmpty = 32,   // + raw stage
+  kBarCount = 40
+};
+constexpr int kOffTmemSlot = kBarCount * 8;
+constexpr int kOffAbort = kOffTmemSlot + 8;
+
+struct PrefillArgs {
+  void* o;
+  const uint8_t* k_scale;  // q4_0 only: fp16 scale planes [B, Hkv, Sk, D/32]
+  const uint8_t* v_scale;
+  int32_t* rescale_count;  // optional [B, Hq, Sq]
+  int B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, n_qtiles;
+  float scale_log2;
+};
+
+// ------------------------------------------------------------------------------------------
+// q4_0 nibble pair -> f16/bf16 pair
+// ------------------------------------------------------------------------------------------
+template <bool BF16>
+struct Dq;
+template <>
+struct Dq<false> {
+  // low nibbles at bits 0-3 / 16-19 -> (n - 8) exactly
+  static __device__ __forceinline__ __half2 lo(uint32_t w) {
+    uint32_t x = (w & 0x000F000Fu) | 0x64006400u;  // 1024 + n
+    return __hsub2(*reinterpret_cast<__half2*>(&x), __halves2half2(__ushort_as_half(0x6408),
+                                                                    __ushort_as_half(0x6408)));
+  }
+  // high nibbles at bits 4-7 / 20-23 -> (n - 8) exactly
+  static __device__ __forceinline__ __half2 hi(uint32_t w) {
+    uint32_t x = (w & 0x00F000F0u) | 0x64006400u;  // 1024 + 16 n
+    const __half2 s = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+    const __half2 c = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));  // -72
+    return __hfma2(*reinterpret_cast<__half2*>(&x), s, c);
+  }
+  static __device__ __forceinline__ uint32_t scale(__half2 v, __half d) {
+    __half2 r = __hmul2(v, __halves2half2(d, d));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+};
+template <>
+struct Dq<true> {
+  static __device__ __forceinline__ __nv_bfloat162 lo(uint32_t w) {
+    uint32_t x = (w & 0x000F000Fu) | 0x43004300u;  // 128 + n
+    const uint32_t c = 0x43084308u;                 // 136
+    return __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x),
+                   *reinterpret_cast<const __nv_bfloat162*>(&c));
+  }
+  static __device__ __forceinline__ __nv_bfloat162 hi(uint32_t w) {
+    uint32_t x = (w & 0x00F000F0u) | 0x43004300u;  // 128 + 16 n
+    const uint32_t s = 0x3D803D80u;                 // 1/16
+    const uint32_t c = 0xC180C180u;                 // -16
+    return __hfma2(*reinterpret_cast<__nv_bfloat162*>(&x),
+                   *reinterpret_cast<const __nv_bfloat162*>(&s),
+                   *reinterpret_cast<const __nv_bfloat162*>(&c));
+  }
+  static __device__ __forceinline__ uint32_t scale(__nv_bfloat162 v, float d) {
+    // (n - 8) * d rounded once to bf16: the product of a 4-bit integer and an fp16 value is
+    // exact in f32, so round only after the f32 multiply.
+    const float2 f = __bfloat1622float2(v);
+    __nv_bfloat162 r = __floats2bfloat162_rn(f.x * d, f.y * d);
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+};
+
+template <int D, bool BF16, bool Q4>
+__global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
+  using C = Cfg<D, Q4>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffBar + kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::kOffBar + kOffTmemSlot);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // work unit: longest q tiles first (the slowest grid dimension enumerates q tiles)
+  const int h = blockIdx.x;
+  const int b = blockIdx.y;
+  const int qtile = args.n_qtiles - 1 - static_cast<int>(blockIdx.z);
+  const int q0 = qtile * kBM;
+  const int g = h / (args.Hq / args.Hkv);
+  const int last_row = min(q0 + kBM - 1, args.Sq - 1);
+  const int kend = args.causal ? min(args.Sk, args.q_pos_offset + last_row + 1) : args.Sk;
+  const int nb = (kend + kBN - 1) / kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarSFull0), 1);
+    mbar_init(bar(kBarSFull1), 1);
+    mbar_init(bar(kBarPReady0), 128);
+    mbar_init(bar(kBarPReady1), 128);
+    mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarDrain), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(kBarRingFull + s), Q4 ? 128 : 1);
+      mbar_init(bar(kBarRingEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kRawStages; ++s) {
+      mbar_init(bar(kBarRawFull + s), 1 + 32);  // TMA lane + 32 cp.async arrivals
+      mbar_init(bar(kBarRawEmpty + s), 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+    }
+    bool ok = true;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(kBarQFull), C::kQBytes);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sbase + C::kOffQ + c * (kBM * 128), &tm_q, bar(kBarQFull), c * 64, q0,
+                    b * args.Hq + h);
+    }
+    // tiles in the order the MMA consumes them: K0, K1, V0, K2, V1, K3, ...
+    int n = 0;
+    auto produce = [&](bool is_v, int j) {
+      if (!ok) return;
+      if constexpr (!Q4) {
+        const int s = n % C::kStages;
+        if (lane == 0) {
+          if (n >= C::kStages)
+            ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                           &g_prefill_error);
+          if (ok) {
+            mbar_arrive_expect_tx(bar(kBarRingFull + s), C::kTileBytes);
+            const uint32_t dst = sbase + C::kOffRing + s * C::kTileBytes;
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(dst + c * (kBN * 128), is_v ? &tm_v : &tm_k, bar(kBarRingFull + s),
+                          c * 64, j * kBN, b * args.Hkv + g);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      } else {
+        const int s = n % C::kRawStages;
+        if (n >= C::kRawStages) {
+          if (lane == 0)
+            ok = mbar_wait(bar(kBarRawEmpty + s), ((n / C::kRawStages) - 1) & 1, abort_flag,
+                           &g_prefill_error);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) return;
+        }
+        const uint32_t dst = sbase + C::kOffRaw + s * C::kRawBytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(kBarRawFull + s), C::kRawNib);
+          tma_load_3d(dst, is_v ? &tm_v : &tm_k, bar(kBarRawFull + s), 0, j * kBN,
+                      b * args.Hkv + g);
+        }
+        // scales: one 4- or 8-byte row per key, zero-filled past Sk
+        const uint8_t* sp = is_v ? args.v_scale : args.k_scale;
+        for (int r = lane; r < kBN; r += 32) {
+          const int key = j * kBN + r;
+          const bool in = key < args.Sk;
+          const uint8_t* src =
+              sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Sk + (in ? key : 0)) *
+                       C::kScaleRow;
+          const uint32_t d = dst + C::kRawNib + r * C::kScaleRow;
+          if (C::kScaleRow == 8)
+            cp_async_8(d, src, in ? 8u : 0u);
+          else
+            cp_async_4(d, src, in ? 4u : 0u);
+        }
+        cp_async_mbar_arrive_noinc(bar(kBarRawFull + s));
+      }
+      ++n;
+    };
+    produce(false, 0);
+    if (nb > 1) produce(false, 1);
+    for (int j = 0; j < nb; ++j) {
+      produce(true, j);
+      if (j + 2 < nb) produce(false, j + 2);
+    }
+    if (!ok && lane == 0) {
+      // let copies already issued land before the CTA's shared memory goes away
+      volatile int never = 0;
+      constexpr int stages = Q4 ? C::kRawStages : C::kStages;
+      for (int i = max(0, n - stages); i < n; ++i) {
+        const int s = i % stages;
+        mbar_wait(bar((Q4 ? kBarRawFull : kBarRingFull) + s), (i / stages) & 1, &never, nullptr,
+                  kWaitLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc_f16(kBM, kBN, BF16, false);
+      constexpr uint32_t idesc_pv = make_idesc_f16(kBM, D, BF16, true);
+      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, &g_prefill_error);
+      tc_fence_after();
+      const uint32_t qaddr = sbase + C::kOffQ;
+      int n = 0;
+      auto acquire = [&]() -> int {
+        const int s = n % C::kStages;
+        if (ok) ok = mbar_wait(bar(kBarRingFull + s), (n / C::kStages) & 1, abort_flag,
+                               &g_prefill_error);
+        tc_fence_after();
+        return s;
+      };
+      auto release = [&](int s) {
+        mma_commit(bar(kBarRingEmpty + s));
+        ++n;
+      };
+      auto issue_qk = [&](int j) {
+        const int s = acquire();
+        if (!ok) return;
+        const uint32_t kaddr = sbase + C::kOffRing + s * C::kTileBytes;
+        const uint32_t dcol = tmem + ((j & 1) ? kColS1 : kColS0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          const uint64_t ad = make_sdesc_sw128(qaddr + off, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(kaddr + off, 16, 1024);
+          mma_ss(dcol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        release(s);
+        mma_commit(bar((j & 1) ? kBarSFull1 : kBarSFull0));
+      };
+      auto issue_pv = [&](int j) {
+        const int s = acquire();
+        if (!ok) return;
+        ok = mbar_wait(bar((j & 1) ? kBarPReady1 : kBarPReady0), (j >> 1) & 1, abort_flag,
+                       &g_prefill_error);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
+        const uint32_t pcol = tmem + ((j & 1) ? kColS1 : kColS0);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t bd = make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024);
+          mma_ts(tmem + kColO, pcol + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        release(s);
+        mma_commit(bar(kBarODone));
+      };
+      if (ok) issue_qk(0);
+      if (ok && nb > 1) issue_qk(1);
+      for (int j = 0; j < nb && ok; ++j) {
+        issue_pv(j);
+        if (ok && j + 2 < nb) issue_qk(j + 2);
+      }
+      if (!ok) {
+        // wait until every MMA issued so far has finished before TMEM is released
+        volatile int never = 0;
+        mma_commit(bar(kBarDrain));
+        mbar_wait(bar(kBarDrain), 0, &never, nullptr, kWaitLimitNs);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- softmax rows
+    const int row = 32 * (warp & 3) + lane;
+    const int qrow = q0 + row;
+    const int pos = args.q_pos_offset + qrow;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const float sl2 = args.scale_log2;
+    float f = -INFINITY;  // frame, base-2 units of the scaled score
+    float l = 0.f;
+    int nres = 0;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const uint32_t scol = (j & 1) ? kColS1 : kColS0;
+      ok = mbar_wait(bar((j & 1) ? kBarSFull1 : kBarSFull0), (j >> 1) & 1, abort_flag,
+                     &g_prefill_error);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float s[kBN];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          tmem_ld32(tmem + lane_off + scol + 32 * c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
+        }
+      }
+      const int kb = j * kBN;
+      const bool need_mask =
+          (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
+      if (need_mask) {
+        const int lim = args.causal ? min(args.Sk - 1, pos) : args.Sk - 1;
+#pragma unroll
+        for (int i = 0; i < kBN; ++i)
+          if (kb + i > lim) s[i] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      const float m2 = mx * sl2;
+      const bool need = m2 > f + kMarginLog2;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2(f - m2) : 1.f;
+        if (need) {
+          l *= alpha;
+          f = m2;
+          ++nres;
+        }
+        if (j > 0) {
+          // O holds the blocks before j; PV(j-1) must have landed before it is rescaled
+          ok = mbar_wait(bar(kBarODone), (j - 1) & 1, abort_flag, &g_prefill_error);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + kColO + 32 * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tmem + lane_off + kColO + 32 * c, r);
+          }
+          tmem_wait_st();
+        }
+      }
+      const float nf = -f;
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t pr[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(s[32 * c + 2 * i], sl2, nf));
+          const float p1 = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, nf));
+          l += p0 + p1;
+          pr[i] = pack2<BF16>(p0, p1);
+        }
+        tmem_st16(tmem + lane_off + scol + 16 * c, pr);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar((j & 1) ? kBarPReady1 : kBarPReady0));
+    }
+    if (ok) {
+      ok = mbar_wait(bar(kBarODone), (nb - 1) & 1, abort_flag, &g_prefill_error);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool store = qrow < args.Sq;
+      uint8_t* orow = static_cast<uint8_t*>(args.o) +
+                      ((static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow) * D) * 2;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kColO + 32 * c, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv_l,
+                              __uint_as_float(r[2 * i + 1]) * inv_l);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (store && args.rescale_count)
+        args.rescale_count[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = nres;
+    }
+  } else if constexpr (Q4) {
+    // ---------------------------------------------------------------- q4_0 dequant
+    // thread t expands key row t of each raw tile into the 128B-swizzled f16/bf16 ring stage
+    const int t = threadIdx.x - 6 * 32;
+    bool ok = true;
+    const int ntiles = 2 * nb;
+    for (int n = 0; n < ntiles; ++n) {
+      const int rs = n % C::kRawStages;
+      const int s = n % C::kStages;
+      ok = mbar_wait(bar(kBarRawFull + rs), (n / C::kRawStages) & 1, abort_flag,
+                     &g_prefill_error);
+      if (ok && n >= C::kStages)
+        ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                       &g_prefill_error);
+      if (!ok) break;
+      const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
+      const uint8_t* nrow = raw + t * C::kNibRow;
+      const __half* srow = reinterpret_cast<const __half*>(raw + C::kRawNib + t * C::kScaleRow);
+      uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
+#pragma unroll
+      for (int blk = 0; blk < D / 32; ++blk) {
+        // 16 bytes of nibbles of this key, 64B-swizzled (D=128) or 32B-swizzled (D=64) by TMA
+        const int chunk = (D == 128) ? (blk ^ ((t >> 1) & 3)) : (blk ^ ((t >> 2) & 1));
+        const uint4 wv = *reinterpret_cast<const uint4*>(nrow + 16 * chunk);
+        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+        const __half dh = srow[blk];
+        uint32_t outv[16];  // 32 dequantized elements, packed in pairs, natural order
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // bytes 4q..4q+3 -> elements 4q..4q+3 (low) and 4q+16..4q+19 (high)
+          const uint32_t a = __byte_perm(w[q], 0u, 0x5150);  // byte0 at b0, byte1 at b2
+          const uint32_t c2 = __byte_perm(w[q], 0u, 0x5352); // byte2 at b0, byte3 at b2
+          if (BF16) {
+            const float d = __half2float(dh);
+            outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a), d);
+            outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2), d);
+            outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a), d);
+            outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2), d);
+          } else {
+            outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a), dh);
+            outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2), dh);
+            outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a), dh);
+            outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2), dh);
+          }
+        }
+        // elements 32 blk + 8 cc .. +7 form 16-byte chunk (4 blk + cc) of the row
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int col16 = 4 * blk + cc;       // 16-byte chunk index along D
+          const int atom = col16 >> 3;          // 64-element swizzle atom
+          const int ch = (col16 & 7) ^ (t & 7); // 128B swizzle
+          *reinterpret_cast<uint4*>(dst + atom * (kBN * 128) + t * 128 + ch * 16) =
+              make_uint4(outv[4 * cc], outv[4 * cc + 1], outv[4 * cc + 2], outv[4 * cc + 3]);
+        }
+      }
+      // generic-proxy writes must be visible to the tensor core's async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(bar(kBarRingFull + s));
+      mbar_arrive(bar(kBarRawEmpty + rs));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------
+// host launch
+// ------------------------------------------------------------------------------------------
+template <int D, bool BF16, bool Q4>
+static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
+  using C = Cfg<D, Q4>;
+  static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
+  auto kern = prefill_kernel<D, BF16, Q4>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  PrefillArgs a;
+  a.o = L.o;
+  a.k_scale = static_cast<const uint8_t*>(L.k_scale);
+  a.v_scale = static_cast<const uint8_t*>(L.v_scale);
+  a.rescale_count = L.rescale_count;
+  a.B = L.B;
+  a.Hq = L.Hq;
+  a.Hkv = L.Hkv;
+  a.Sq = L.Sq;
+  a.Sk = L.Sk;
+  a.q_pos_offset = L.q_pos_offset;
+  a.causal = L.causal;
+  a.n_qtiles = (L.Sq + kBM - 1) / kBM;
+  a.scale_log2 = L.scale * kLog2e;
+  dim3 grid(L.Hq, L.B, a.n_qtiles);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, a);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream) {
+  if (L.D == 128) {
+    if (L.q4) return L.bf16 ? launch_t<128, true, true>(L, stream) : launch_t<128, false, true>(L, stream);
+    return L.bf16 ? launch_t<128, true, false>(L, stream) : launch_t<128, false, false>(L, stream);
+  }
+  if (L.q4) return L.bf16 ? launch_t<64, true, true>(L, stream) : launch_t<64, false, true>(L, stream);
+  return L.bf16 ? launch_t<64, true, false>(L, stream) : launch_t<64, false, false>(L, stream);
+}
+
+uint32_t prefill_take_error() {
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  const uint32_t z = 0;
+  cudaMemcpyToSymbol(g_prefill_error, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fa

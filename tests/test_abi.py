@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, exports every
+function include/fa.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import quantized_kv_cache_sm_gb300 as fa
+from quantized_kv_cache_sm_gb300 import build as fa_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert set(declared_functions()) == set(fa.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa_build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s+(fa_[a-z0-9_]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings_and_version(lib):
+    assert fa.fa_status_string(0) == "FA_OK"
+    assert fa.fa_status_string(4) == "FA_ERR_TIMEOUT"
+    assert fa.fa_version() == 100
+
+
+def test_q4_0_sizes(lib):
+    # [B, H, S, D] = [1, 8, 16384, 128]: 8 MiB of nibbles, scale plane right after (aligned)
+    assert fa.fa_q4_0_scale_offset(1, 8, 16384, 128) == 8 * 16384 * 64
+    assert fa.fa_q4_0_bytes(1, 8, 16384, 128) == 8 * 16384 * 64 + 8 * 16384 * 4 * 2
+    # 4.5 bits per element: the "about 75% smaller" cache of the q4_0 page is 71.9% smaller
+    assert fa.fa_q4_0_bytes(4, 8, 65536, 128) == 4 * 8 * 65536 * 72  # K or V: 72 B per row
+    # the scale plane starts at a 256-byte boundary
+    off = fa.fa_q4_0_scale_offset(1, 1, 3, 32)
+    assert off == 256 and fa.fa_q4_0_bytes(1, 1, 3, 32) == 256 + 3 * 2
+    assert fa.fa_q4_0_bytes(1, 1, 1, 48) == 0  # D must be a multiple of 32
+
+
+def test_workspace_is_zero_for_prefill(lib):
+    assert fa.fa_workspace_bytes(1, 32, 8, 2048, 16384, 128, 14336, 1) == 0
+    assert fa.fa_workspace_bytes(1, 32, 7, 2, 16, 128, 0, 1) == 0  # invalid: Hq % Hkv
+
+
+P = 1 << 20  # a 16-byte aligned fake device address; never dereferenced by these calls
+
+
+@pytest.mark.parametrize("args,expect", [
+    # q, k, v, o, B, Hq, Hkv, Sq, Sk, D, off, causal, scale, dtype, kv
+    ((0, P, P, P, 1, 8, 8, 4, 4, 64, 0, 1, 0.125, 0, 0), fa.FA_ERR_INVALID_ARG),   # null q
+    ((P + 2, P, P, P, 1, 8, 8, 4, 4, 64, 0, 1, 0.125, 0, 0), fa.FA_ERR_INVALID_ARG),  # misaligned
+    ((P, P, P, P, 0, 8, 8, 4, 4, 64, 0, 1, 0.125, 0, 0), fa.FA_ERR_INVALID_ARG),   # B = 0
+    ((P, P, P, P, 1, 8, 3, 4, 4, 64, 0, 1, 0.125, 0, 0), fa.FA_ERR_INVALID_ARG),   # Hq % Hkv
+    ((P, P, P, P, 1, 8, 8, 4, 4, 64, 1, 1, 0.125, 0, 0), fa.FA_ERR_INVALID_ARG),   # off+Sq > Sk
+    ((P, P, P, P, 1, 8, 8, 4, 4, 64, -1, 1, 0.125, 0, 0), fa.FA_ERR_INVALID_ARG),  # off < 0
+    ((P, P, P, P, 1, 8, 8, 4, 4, 64, 0, 1, 0.0, 0, 0), fa.FA_ERR_INVALID_ARG),     # scale 0
+    ((P, P, P, P, 1, 8, 8, 4, 4, 64, 0, 1, float("nan"), 0, 0), fa.FA_ERR_INVALID_ARG),
+    ((P, P, P, P, 1, 8, 8, 4, 4, 64, 0, 1, 0.125, 2, 0), fa.FA_ERR_INVALID_ARG),   # dtype
+    ((P, P, P, P, 1, 8, 8, 4, 4, 64, 0, 1, 0.125, 0, 5), fa.FA_ERR_INVALID_ARG),   # kv format
+    ((P, P, P, P, 1, 8, 8, 4, 4, 96, 0, 1, 0.125, 0, 0), fa.FA_ERR_UNSUPPORTED),   # D = 96
+    ((P, P, P, P, 1, 16, 1, 1, 4, 64, 3, 1, 0.125, 0, 0), fa.FA_ERR_UNSUPPORTED),  # decode G > 8
+])
+def test_bad_arguments_rejected_on_host(lib, args, expect):
+    assert lib.fa_fwd(*args, None) == expect
+    assert lib.fa_fwd_ex(*args, None, 0, None, None) == expect
+
+
+def test_decode_without_workspace_rejected(lib):
+    # Sq == 1 needs scratch; fa_fwd_ex with none is an argument error (checked before launch)
+    need = lib.fa_workspace_bytes(1, 8, 2, 1, 4096, 128, 4095, 1)
+    if need == 0:
+        pytest.skip("no device to size the split")
+    st = lib.fa_fwd_ex(P, P, P, P, 1, 8, 2, 1, 4096, 128, 4095, 1, 0.088, 0, 0, None, 0, None,
+                       None)
+    assert st == fa.FA_ERR_INVALID_ARG
+
+
+def test_quantize_bad_arguments(lib):
+    assert lib.fa_quantize_q4_0(P, P, 1, 1, 1, 48, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_quantize_q4_0(0, P, 1, 1, 1, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_quantize_q4_0(P, P + 8, 1, 1, 1, 64, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_quantize_q4_0(P, P, 1, 1, 1, 64, 7, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        fa.load_from(str(tmp_path / "missing.so"))

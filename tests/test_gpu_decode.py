@@ -1,0 +1,76 @@
+"""Split-K decode (Sq == 1) against the f64 oracle, through the C ABI: every output element."""
+import numpy as np
+import pytest
+import torch
+
+import fa_inputs
+import oracle
+from gpu_common import check_close, np64, oracle_q4_planes
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode(fa, B, Hq, Hkv, Sk, D, causal, off, dtype, kv, seed, use_ws=True):
+    q, k, v = fa_inputs.make_tensors(B, Hq, Hkv, 1, Sk, D, dtype, seed=seed)
+    scale = D ** -0.5
+    qd = q.cuda()
+    ws = None
+    if use_ws:
+        nbytes = fa.fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, off, causal)
+        assert nbytes > 0
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    if kv == "q4_0":
+        kd, vd = fa.fa_quantize_q4_0(k.cuda()), fa.fa_quantize_q4_0(v.cuda())
+    else:
+        kd, vd = k.cuda(), v.cuda()
+    if use_ws:
+        o = fa.fa_fwd_ex(qd, kd, vd, causal=causal, q_pos_offset=off, scale=scale, workspace=ws)
+    else:
+        o = fa.fa_fwd(qd, kd, vd, causal=causal, q_pos_offset=off, scale=scale)
+    assert fa.fa_get_status() == fa.FA_OK
+    if kv == "q4_0":
+        want = oracle.attention_q4_0(np64(q), oracle_q4_planes(k), oracle_q4_planes(v),
+                                     causal=causal, q_pos_offset=off, scale=scale)
+    else:
+        want = oracle.attention(np64(q), np64(k), np64(v), causal=causal, q_pos_offset=off,
+                                scale=scale)
+    return check_close(np64(o), want, dtype, f"decode B{B} H{Hq}/{Hkv} Sk{Sk} D{D} {dtype} {kv}")
+
+
+CASES = [
+    # B, Hq, Hkv, Sk, D, causal, off, dtype, kv
+    (1, 8, 2, 1, 128, True, 0, "f16", "q4_0"),          # a single key: O = V[0]
+    (1, 8, 2, 100, 128, True, 99, "f16", "q4_0"),
+    (2, 32, 8, 4097, 128, True, 4096, "f16", "q4_0"),
+    (3, 4, 4, 3000, 64, True, 2999, "bf16", "q4_0"),
+    (1, 16, 2, 9999, 128, True, 5000, "f16", "q4_0"),  # keys past the position are masked
+    (2, 8, 1, 2048, 128, False, 0, "bf16", "q4_0"),
+    (1, 6, 2, 777, 64, True, 776, "f16", "q4_0"),       # group of 3
+    (1, 8, 2, 100, 128, True, 99, "f16", "dense"),
+    (2, 32, 8, 4097, 128, True, 4096, "bf16", "dense"),
+    (1, 4, 4, 3000, 64, True, 2999, "f16", "dense"),
+    (1, 8, 1, 5000, 128, False, 0, "f16", "dense"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_decode_small(fa, case):
+    run_decode(fa, *case, seed=11)
+
+
+def test_decode_q4_0_b4_sk65536_full(fa):
+    w = fa_inputs.WORKLOADS["decode_q4_0_b4_gqa32x8_d128_sk65536_f16"]
+    run_decode(fa, w.B, w.Hq, w.Hkv, w.Sk, w.D, True, w.q_pos_offset, w.dtype, "q4_0", w.seed)
+
+
+def test_decode_allocating_entry_point(fa):
+    run_decode(fa, 2, 8, 2, 3000, 128, True, 2999, "f16", "q4_0", seed=12, use_ws=False)
+
+
+def test_decode_ex_rejects_small_workspace(fa):
+    q, k, v = fa_inputs.make_tensors(1, 8, 2, 1, 4096, 128, "f16", seed=1, device="cuda")
+    need = fa.fa_workspace_bytes(1, 8, 2, 1, 4096, 128, 4095, True)
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd_ex(q, k, v, workspace=ws)
+    assert e.value.status == fa.FA_ERR_INVALID_ARG

@@ -1,0 +1,123 @@
+"""Prefill kernel (Sq >= 2) against the f64 oracle, through the C ABI.
+
+Small and ragged shapes are compared on every output element; the full-size chunked-prefill
+workloads on sampled rows (tile edges, last rows, random rows of every head) in the same launch
+configuration the benchmark times.  Tolerance: max-abs 1e-2 (f16) / 2e-2 (bf16)."""
+import numpy as np
+import pytest
+import torch
+
+import fa_inputs
+import oracle
+from gpu_common import check_close, np64, oracle_q4_planes, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(fa, B, Hq, Hkv, Sq, Sk, D, causal, off, dtype, kv, seed, rows=None, ramp=False,
+             counts=False):
+    q, k, v = fa_inputs.make_tensors(B, Hq, Hkv, Sq, Sk, D, dtype, seed=seed, ramp=ramp)
+    scale = D ** -0.5
+    qd = q.cuda()
+    rc = torch.full((B, Hq, Sq), -1, dtype=torch.int32, device="cuda") if counts else None
+    if kv == "q4_0":
+        kq = fa.fa_quantize_q4_0(k.cuda())
+        vq = fa.fa_quantize_q4_0(v.cuda())
+        o = fa.fa_fwd_ex(qd, kq, vq, causal=causal, q_pos_offset=off, scale=scale,
+                         rescale_count=rc)
+        kp, vp = oracle_q4_planes(k), oracle_q4_planes(v)
+        want = oracle.attention_q4_0(np64(q), kp, vp, causal=causal, q_pos_offset=off,
+                                     scale=scale, rows=rows)
+    else:
+        o = fa.fa_fwd_ex(qd, k.cuda(), v.cuda(), causal=causal, q_pos_offset=off, scale=scale,
+                         rescale_count=rc)
+        want = oracle.attention(np64(q), np64(k), np64(v), causal=causal, q_pos_offset=off,
+                                scale=scale, rows=rows)
+    assert fa.fa_get_status() == fa.FA_OK
+    got = np64(o)
+    if rows is not None:
+        got = got.reshape(-1, D)[rows]
+    err = check_close(got, want, dtype, f"B{B} H{Hq}/{Hkv} Sq{Sq} Sk{Sk} D{D} {dtype} {kv}")
+    return err, (rc.cpu().numpy() if counts else None)
+
+
+SMALL = [
+    # B, Hq, Hkv, Sq, Sk, D, causal, off, dtype, kv
+    (1, 4, 2, 200, 200, 128, True, 0, "f16", "dense"),
+    (2, 4, 4, 130, 333, 64, True, 203, "f16", "dense"),
+    (1, 8, 2, 64, 1000, 128, True, 936, "bf16", "dense"),
+    (1, 2, 2, 300, 257, 128, False, 0, "f16", "dense"),
+    (1, 3, 1, 128, 128, 64, True, 0, "bf16", "dense"),
+    (1, 2, 1, 2, 5, 128, True, 3, "f16", "dense"),
+    (1, 4, 2, 100, 500, 128, True, 123, "f16", "dense"),
+    (1, 2, 1, 257, 640, 64, False, 0, "bf16", "dense"),
+    (1, 4, 2, 200, 450, 128, True, 250, "f16", "q4_0"),
+    (1, 2, 1, 130, 130, 64, True, 0, "bf16", "q4_0"),
+    (2, 4, 1, 77, 301, 128, False, 0, "f16", "q4_0"),
+    (1, 2, 2, 3, 1027, 128, True, 1024, "bf16", "q4_0"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "-".join(map(str, c)))
+def test_prefill_small_full_compare(fa, case):
+    run_case(fa, *case, seed=7)
+
+
+def test_selfattn_b2_s512_h8_d64_full(fa):
+    w = fa_inputs.WORKLOADS["selfattn_b2_s512_h8_d64_f16"]
+    err, _ = run_case(fa, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True, 0, w.dtype, "dense", w.seed)
+    assert err < 5e-3
+
+
+def test_chunked_prefill_2k_full(fa):
+    w = fa_inputs.WORKLOADS["prefill_gqa32x8_d128_sq2048_sk2048_f16"]
+    run_case(fa, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True, w.q_pos_offset, w.dtype, "dense",
+             w.seed)
+
+
+@pytest.mark.parametrize("name", ["prefill_gqa32x8_d128_sq2048_sk8192_f16",
+                                  "prefill_gqa32x8_d128_sq2048_sk8192_bf16",
+                                  "prefill_gqa32x8_d128_sq2048_sk16384_f16",
+                                  "prefill_gqa32x8_d128_sq2048_sk16384_bf16",
+                                  "prefill_q4_0_gqa32x8_d128_sq2048_sk16384_f16"])
+def test_chunked_prefill_long_sampled(fa, name):
+    w = fa_inputs.WORKLOADS[name]
+    rows = sample_rows(w.B, w.Hq, w.Sq, per_head=14, seed=w.Sk)
+    _, counts = run_case(fa, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True, w.q_pos_offset, w.dtype,
+                         w.kv_format, w.seed, rows=rows, counts=True)
+    # N(0,1) scores never outgrow the first block's frame by 10: no deferred rescale fires
+    assert counts.min() >= 1 and counts.max() <= 2
+
+
+@pytest.mark.parametrize("name", ["prefill_gqa32x8_d128_sq2048_sk8192_f16_ramp",
+                                  "prefill_gqa32x8_d128_sq2048_sk16384_f16_ramp"])
+def test_score_ramp_drives_deferred_rescale(fa, name):
+    """A per-key bias rising 2.0 per 128-key block: a row's block max outgrows its frame by the
+    10-point margin about every fifth block, so the deferred O/l rescale runs ~Sk/640 times per
+    row, and the output still matches the oracle."""
+    w = fa_inputs.WORKLOADS[name]
+    rows = sample_rows(w.B, w.Hq, w.Sq, per_head=10, seed=1)
+    _, counts = run_case(fa, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True, w.q_pos_offset, w.dtype,
+                         "dense", w.seed, rows=rows, ramp=True, counts=True)
+    nblocks = (w.q_pos_offset + np.arange(w.Sq)) // 128 + 1      # key blocks each row sees
+    per_row = counts.reshape(-1, w.Sq)
+    assert (per_row >= 2).all(), "the deferred rescale branch never ran on some row"
+    expect = 1 + (nblocks - 1) / 5.0
+    ratio = per_row / expect[None, :]
+    assert 0.7 < ratio.mean() < 1.3, ratio.mean()
+    assert ratio.min() > 0.5 and ratio.max() < 1.6
+
+
+def test_fa_fwd_allocating_equals_ex(fa):
+    q, k, v = fa_inputs.make_tensors(1, 4, 2, 256, 512, 128, "f16", seed=3, device="cuda")
+    o1 = fa.fa_fwd(q, k, v)
+    o2 = fa.fa_fwd_ex(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+def test_status_after_many_calls(fa):
+    q, k, v = fa_inputs.make_tensors(1, 8, 2, 512, 4096, 128, "bf16", seed=5, device="cuda")
+    for _ in range(20):
+        fa.fa_fwd(q, k, v)
+    assert fa.fa_get_status() == fa.FA_OK
