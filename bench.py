@@ -57,6 +57,31 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def source_sha16(files) -> str:
+    import hashlib
+
+    m = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "quantized_kv_cache_sm_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def measured_traffic(kernel_key: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel's sources
+    changed since that capture (or no capture exists for this workload)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for ln in open(path):
+        parts = ln.split()
+        if len(parts) >= 5 and not ln.startswith("#") and parts[0] == kernel_key \
+                and parts[4] == workload:
+            if source_sha16(parts[1].split("+")) == parts[2]:
+                return int(parts[3])
+    return None
+
+
 def kv_bytes_q4_0(w: fa_inputs.Workload) -> int:
     """Algorithmic K+V bytes one decode call reads: every visible key of every (b, kv head),
     nibbles (D/2 bytes) + fp16 scales (D/32 * 2 bytes), for K and for V."""
@@ -254,7 +279,8 @@ def run_ours(args, rank, world, local_rank):
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
             "peak_source": f"{peaks_src} bf16 dense burst (f16 runs at the same rate)",
-            "traffic": None,
+            "traffic": measured_traffic(f"prefill_kernel_{w.dtype}_{w.kv_format}", w.name),
+            "traffic_unit": "bytes per launch (ncu dram read + write)",
             "algorithmic_flops_per_launch": flops,
         },
         "gpu_launches": args.steps,
@@ -327,7 +353,8 @@ def decode_leg(fa, dev, stream, peaks, peaks_src):
         "roofline": {"kernel": "decode_split_kernel + decode_combine_kernel (one call)",
                      "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                     "peak_source": f"{peaks_src} HBM copy", "traffic": None},
+                     "peak_source": f"{peaks_src} HBM copy",
+                     "traffic": measured_traffic("decode_split_kernel_f16_q4_0", w.name)},
     }
 
 

@@ -100,14 +100,11 @@ __device__ __forceinline__ uint32_t nib_lo(uint32_t w) {
 }
 template <bool BF16>
 __device__ __forceinline__ uint32_t nib_hi(uint32_t w) {
-  uint32_t x = (w & 0x00F000F0u) | (BF16 ? 0x43004300u : 0x64006400u);
   if (BF16) {
-    const uint32_t s = 0x3D803D80u, c = 0xC180C180u;  // 1/16, -16
-    __nv_bfloat162 r = __hfma2(*reinterpret_cast<__nv_bfloat162*>(&x),
-                               *reinterpret_cast<const __nv_bfloat162*>(&s),
-                               *reinterpret_cast<const __nv_bfloat162*>(&c));
-    return *reinterpret_cast<uint32_t*>(&r);
+    // bf16 has 7 mantissa bits: a high nibble at bits 4-7 would reach the exponent
+    return nib_lo<true>(w >> 4);
   } else {
+    uint32_t x = (w & 0x00F000F0u) | 0x64006400u;     // 1024 + 16 n
     const uint32_t s = 0x2C002C00u, c = 0xD480D480u;  // 1/16, -72
     __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<const __half2*>(&s),
                         *reinterpret_cast<const __half2*>(&c));

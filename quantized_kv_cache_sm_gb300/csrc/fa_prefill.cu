@@ -120,14 +120,9 @@ struct Dq<true> {
     return __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x),
                    *reinterpret_cast<const __nv_bfloat162*>(&c));
   }
-  static __device__ __forceinline__ __nv_bfloat162 hi(uint32_t w) {
-    uint32_t x = (w & 0x00F000F0u) | 0x43004300u;  // 128 + 16 n
-    const uint32_t s = 0x3D803D80u;                 // 1/16
-    const uint32_t c = 0xC180C180u;                 // -16
-    return __hfma2(*reinterpret_cast<__nv_bfloat162*>(&x),
-                   *reinterpret_cast<const __nv_bfloat162*>(&s),
-                   *reinterpret_cast<const __nv_bfloat162*>(&c));
-  }
+  // bf16 has 7 mantissa bits, so a high nibble at bits 4-7 would reach the exponent: shift it
+  // down to bits 0-3 first
+  static __device__ __forceinline__ __nv_bfloat162 hi(uint32_t w) { return lo(w >> 4); }
   static __device__ __forceinline__ uint32_t scale(__nv_bfloat162 v, float d) {
     // (n - 8) * d rounded once to bf16: the product of a 4-bit integer and an fp16 value is
     // exact in f32, so round only after the f32 multiply.
