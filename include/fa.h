@@ -93,6 +93,33 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
 size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
                           int causal);
 
+/* Size of the fixed scratch area behind fa_fwd_decode_noalloc (4 MiB). */
+#define FA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* Decode (one query token per sequence, Sq = 1) that allocates no device memory.
+ * The pages have no counterpart of this entry point: it exists for callers that cannot allocate
+ * on the call path -- runtimes that reserve all device memory at start-up and manage it
+ * themselves, or hosts that forbid allocation once serving has started because an allocation
+ * may block on the device.  fa_fwd takes decode scratch from the stream-ordered allocator and
+ * fa_fwd_ex needs a caller-provided buffer; this call instead uses a fixed device array of
+ * FA_NOALLOC_SCRATCH_BYTES that the library itself holds on every GPU that loads it, until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  Arguments: as fa_fwd with Sq = 1 (q, o: [B, Hq, 1, D]; k, v: [B, Hkv, Sk, D] dense or q4_0).
+ *  Limit: shapes whose fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal) exceeds
+ *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED (for D = 128 that is
+ *    B * Hq * nsplit > 7943, nsplit being the split count the decode plan picks, at most
+ *    4 * SM count / (B * Hkv) rounded, at least 1); invalid shapes give FA_ERR_INVALID_ARG.
+ *  First call per device: it looks up the array's device address (cudaGetSymbolAddress) with
+ *    that device current, so make the first call on each device before any stream capture.
+ *  Sharing: every call on a device uses the same array and leaves its contents behind.  Nothing
+ *    in it needs clearing (each call writes every entry it later reads), but calls whose
+ *    execution overlaps on the GPU -- on different streams, or from different host threads --
+ *    race on the array and produce wrong results; order them on one stream or with events. */
+fa_status fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, int B,
+                                int Hq, int Hkv, int Sk, int D, int q_pos_offset, int causal,
+                                float scale, fa_dtype dtype, fa_kv_format kv_format,
+                                fa_stream_t stream);
+
 /* Size in bytes of a q4_0 tensor for a [B, H, S, D] source, and the offset of its scale plane. */
 size_t fa_q4_0_bytes(int B, int H, int S, int D);
 size_t fa_q4_0_scale_offset(int B, int H, int S, int D);

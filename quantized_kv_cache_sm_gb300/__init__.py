@@ -25,7 +25,7 @@ FA_KV_DENSE, FA_KV_Q4_0 = 0, 1
 EXPORTED = (
     "fa_fwd", "fa_fwd_ex", "fa_workspace_bytes", "fa_q4_0_bytes", "fa_q4_0_scale_offset",
     "fa_quantize_q4_0", "fa_get_status", "fa_status_string", "fa_debug_wait_timeout",
-    "fa_version",
+    "fa_version", "fa_fwd_decode_noalloc",
 )
 
 _lib = None
@@ -77,6 +77,8 @@ def load_from(p: str) -> ctypes.CDLL:
     lib.fa_debug_wait_timeout.restype = i
     lib.fa_version.argtypes = []
     lib.fa_version.restype = i
+    lib.fa_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_decode_noalloc.restype = i
     return lib
 
 
@@ -242,3 +244,19 @@ def fa_debug_wait_timeout(limit_ns: int, stream=None) -> None:
 
 def fa_version() -> int:
     return int(load().fa_version())
+
+
+def fa_fwd_decode_noalloc(q, k, v, o=None, *, causal: bool = True,
+                          q_pos_offset: int | None = None, scale: float | None = None,
+                          stream=None) -> torch.Tensor:
+    """Decode (Sq = 1) without any device allocation by the library: the split-K scratch comes
+    from a fixed area the library keeps on each GPU (FA_NOALLOC_SCRATCH_BYTES), for callers that
+    must not allocate on the call path.  Calls that overlap on the GPU race on that area."""
+    if o is None:
+        o = torch.empty_like(q)
+    lib = load()
+    a = _fwd_args(q, k, v, o, causal, q_pos_offset, scale)
+    if a[7] != 1:
+        raise ValueError("fa_fwd_decode_noalloc takes one query token per sequence (Sq == 1)")
+    _check(lib.fa_fwd_decode_noalloc(*a[:7], *a[8:], _stream(stream)), "fa_fwd_decode_noalloc")
+    return o

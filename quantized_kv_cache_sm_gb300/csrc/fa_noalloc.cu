@@ -1,0 +1,63 @@
+// Decode entry point that allocates nothing.
+//
+// Some callers cannot allocate device memory on the call path: inference runtimes that reserve
+// the whole HBM pool at start-up and hand out slices themselves (a cudaMalloc or cudaMallocAsync
+// from a library would either fail or fragment their pool), and hosts that forbid any allocation
+// once serving has started because an allocation can block on the device.  fa_fwd needs a few MB
+// of split-K scratch for decode and takes it from the stream-ordered allocator; fa_fwd_ex needs
+// the caller to find that memory.  fa_fwd_decode_noalloc instead uses a fixed scratch area that
+// lives in this file as a `static __device__` array: every GPU that loads the library holds it
+// (FA_NOALLOC_SCRATCH_BYTES) until the process exits.
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr size_t kNoallocScratchBytes = FA_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoallocScratchBytes % 256 == 0, "scratch size");
+
+// The decode split partials of every fa_fwd_decode_noalloc call.  In host code this name is only
+// a stand-in for the device array, never a device address: the address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
+
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o,
+                                           int B, int Hq, int Hkv, int Sk, int D,
+                                           int q_pos_offset, int causal, float scale,
+                                           fa_dtype dtype, fa_kv_format kv_format,
+                                           fa_stream_t stream) {
+  using namespace fa;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    // one-time set-up per device, with that device current: look up where the array lives
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return FA_ERR_CUDA;
+      g_scratch_addr[dev] = p;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  // the scratch this shape needs (0 means the shape itself is invalid)
+  const size_t need = fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal);
+  if (need == 0) return FA_ERR_INVALID_ARG;
+  if (need > kNoallocScratchBytes) return FA_ERR_UNSUPPORTED;
+  // Every partial the combine kernel reads is written earlier in the same call, so the area
+  // needs no clearing between calls.
+  return fa_fwd_ex(q, k, v, o, B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal, scale, dtype,
+                   kv_format, scratch, kNoallocScratchBytes, nullptr, stream);
+}
