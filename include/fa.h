@@ -107,8 +107,8 @@ size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_p
  *  Arguments: as fa_fwd with Sq = 1 (q, o: [B, Hq, 1, D]; k, v: [B, Hkv, Sk, D] dense or q4_0).
  *  Limit: shapes whose fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal) exceeds
  *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED (for D = 128 that is
- *    B * Hq * nsplit > 7943, nsplit being the split count the decode plan picks, at most
- *    4 * SM count / (B * Hkv) rounded, at least 1); invalid shapes give FA_ERR_INVALID_ARG.
+ *    B * Hq * nsplit > 7943, nsplit being the split count the decode plan picks: about
+ *    3 * SM count / (B * Hkv), at least 1); invalid shapes give FA_ERR_INVALID_ARG.
  *  First call per device: it looks up the array's device address (cudaGetSymbolAddress) with
  *    that device current, so make the first call on each device before any stream capture.
  *  Sharing: every call on a device uses the same array and leaves its contents behind.  Nothing

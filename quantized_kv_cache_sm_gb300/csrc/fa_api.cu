@@ -94,15 +94,26 @@ fa_status check_common(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_
   return FA_OK;
 }
 
+// decode scratch of one cache format (0 for Sq >= 2)
 size_t workspace_for(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
-                     int causal, int* nsplit_out, int* chunk_out) {
+                     int causal, bool q4, int* nsplit_out, int* chunk_out) {
   if (Sq != 1) return 0;
   const int sk_eff = causal ? q_pos_offset + 1 : Sk;
   int ns = 1, ck = sk_eff;
-  decode_plan(B, Hkv, sk_eff, num_sms(), &ns, &ck);
+  decode_plan(B, Hkv, sk_eff, num_sms(), q4, &ns, &ck);
   if (nsplit_out) *nsplit_out = ns;
   if (chunk_out) *chunk_out = ck;
   return static_cast<size_t>(B) * Hq * ns * (D + 4) * sizeof(float);
+}
+
+// enough decode scratch for either cache format
+size_t workspace_any(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
+                     int causal) {
+  const size_t a = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, true, nullptr,
+                                 nullptr);
+  const size_t b = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, false, nullptr,
+                                 nullptr);
+  return a > b ? a : b;
 }
 
 }  // namespace
@@ -128,7 +139,7 @@ size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_p
   if (check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, 1.f, FA_F16, FA_KV_DENSE) !=
       FA_OK)
     return 0;
-  return workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, nullptr, nullptr);
+  return workspace_any(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal);
 }
 
 fa_status fa_quantize_q4_0(const void* x, void* out_q4, int B, int H, int S, int D,
@@ -164,21 +175,22 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
   if (Sq == 1) {
     int nsplit = 1, chunk = 1;
     const size_t need =
-        workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, &nsplit, &chunk);
+        workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, q4, &nsplit, &chunk);
+    const uint32_t tile = static_cast<uint32_t>(decode_tile_keys(q4));
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
       return FA_ERR_INVALID_ARG;
     DecodeLaunch L;
     bool ok;
     if (q4) {
-      ok = make_map(&L.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, 64,
+      ok = make_map(&L.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, tile,
                     nib_sw) &&
-           make_map(&L.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, 64,
+           make_map(&L.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, tile,
                     nib_sw);
       L.k_scale = static_cast<const uint8_t*>(k) + kv_scale_off;
       L.v_scale = static_cast<const uint8_t*>(v) + kv_scale_off;
     } else {
-      ok = make_map(&L.tm_k, k, tdt, 2, D, Sk, BHkv, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(&L.tm_v, v, tdt, 2, D, Sk, BHkv, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = make_map(&L.tm_k, k, tdt, 2, D, Sk, BHkv, 64, tile, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&L.tm_v, v, tdt, 2, D, Sk, BHkv, 64, tile, CU_TENSOR_MAP_SWIZZLE_128B);
       L.k_scale = L.v_scale = nullptr;
     }
     if (!ok) return FA_ERR_CUDA;
@@ -240,8 +252,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, in
       check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale, dtype, kv_format);
   if (st != FA_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t need = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, nullptr,
-                                    nullptr);
+  const size_t need = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal,
+                                    kv_format == FA_KV_Q4_0, nullptr, nullptr);
   void* ws = nullptr;
   if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess) return FA_ERR_CUDA;
   const fa_status r = fa_fwd_ex(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale,

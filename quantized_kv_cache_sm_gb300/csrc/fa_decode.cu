@@ -5,15 +5,22 @@
 // Fix It", The Problem table, are where flash attention lost most).  The design follows that:
 //
 //  * grid = (split, kv head, batch); every CTA streams one contiguous key range of one kv head
-//    through a ring of shared-memory stages (TMA for nibble / dense tiles, cp.async for the fp16
-//    scale rows), and all query heads of the GQA group are served from that single read;
+//    through a ring of shared-memory stages (TMA for nibble / dense tiles, bulk copies or
+//    cp.async for the fp16 scale rows), and all query heads of the GQA group are served from that
+//    single read;
 //  * the two contractions are tiny (N = group size <= 8), so they run on mma.sync m16n8k16 with
 //    the *keys* as the M dimension: S^T = K Q^T and O^T += V^T P^T.  The q4_0 nibbles go straight
-//    from shared memory into MMA fragment registers (ldmatrix, LOP3 + HSUB2 to exact (q - 8));
-//    the per-block fp16 scales are applied in f32 on the accumulator for K and folded into P for
-//    V, so no dequantized tile is ever written back;
-//  * each consumer warp keeps its own online softmax state; the warps of a CTA merge through
-//    shared memory and write one partial (m, l, unnormalised O) per query head and split;
+//    from shared memory into MMA fragment registers (ldmatrix + one LOP3 per pair), so no
+//    dequantized tile is ever written back;
+//  * K side: the MMA consumes the raw "magic number" values (1024 + q) and (1024 + 16 q) (f16) or
+//    (128 + q) (bf16); the constant offsets are removed by starting each block's accumulator at
+//    -(offset * sum of the matching Q elements), and the block's fp16 scale is applied in f32 on
+//    the accumulator;
+//  * V side: exact (q - 8) values in the A fragments; the V scales are folded into P, which the
+//    B fragment takes from the S accumulator through movmatrix.trans;
+//  * each consumer warp keeps its own online softmax state over 16 or 32 keys per step; the warps
+//    of a CTA merge through shared memory and write one partial (m, l, unnormalised O) per query
+//    head and split;
 //  * a combine kernel merges the splits: M = max m_s, O = sum e^(m_s - M) O_s / sum e^(m_s - M) l_s.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -24,23 +31,28 @@ __device__ uint32_t g_decode_error;
 
 namespace {
 
-constexpr int kTileKeys = 64;      // keys per stage
-constexpr int kConsumers = 4;      // consumer warps, 16 keys of every tile each
+constexpr int kConsumers = 4;  // consumer warps per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D, bool Q4>
 struct DCfg {
-  static constexpr int kNibBytes = kTileKeys * D / 2;            // q4_0 nibble tile
-  static constexpr int kScaleBytes = kTileKeys * (D / 32) * 2;   // q4_0 scale rows
-  static constexpr int kDenseBytes = kTileKeys * D * 2;          // f16/bf16 tile
+  static constexpr int kSub = Q4 ? 2 : 1;                      // 16-key sub-tiles per warp step
+  static constexpr int kTileKeys = 16 * kSub * kConsumers;     // keys per stage
+  static constexpr int kNB = D / 32;                           // q4_0 blocks per key row
+  static constexpr int kRow = kNB * 2;                         // scale bytes per key row
+  static constexpr int kNibBytes = kTileKeys * D / 2;
+  // scales as the producer leaves them: K as f32 [key][block] (times the softmax scale in base
+  // 2); V as f32 [key][block] (bf16) or as fp16 key pairs [16-key group][t][half][block] (f16)
+  static constexpr int kScaleBytes = kTileKeys * kNB * 4;
+  static constexpr int kDenseBytes = kTileKeys * D * 2;
   static constexpr int kKBytes = Q4 ? kNibBytes : kDenseBytes;
-  // stage: K tile | V tile | K scales | V scales, each region 1024-byte aligned
+  // stage: K tile | V tile | K scales | V scales
   static constexpr int kOffV = (kKBytes + 1023) / 1024 * 1024;
   static constexpr int kOffKs = kOffV + (kKBytes + 1023) / 1024 * 1024;
   static constexpr int kOffVs = kOffKs + (Q4 ? kScaleBytes : 0);
   static constexpr int kStageBytes = ((kOffVs + (Q4 ? kScaleBytes : 0)) + 1023) / 1024 * 1024;
-  static constexpr int kStages = Q4 ? (D == 128 ? 5 : 8) : (D == 128 ? 3 : 5);
-  static constexpr int kCtasPerSm = Q4 ? 4 : 2;
+  static constexpr int kStages = Q4 ? (D == 128 ? 3 : 6) : (D == 128 ? 3 : 6);
+  static constexpr int kCtasPerSm = Q4 ? 3 : 2;
   static constexpr int kOffBar = kStages * kStageBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static constexpr int kThreads = 32 * (1 + kConsumers);
@@ -53,63 +65,108 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
 }
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                           uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
 }
 __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
+}
+// d = A B + c with separate accumulator input and output registers
+template <bool BF16>
+__device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1, float c0,
+                                           float c1, float c2, float c3) {
+  if (BF16)
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2),
+          "f"(c3));
+  else
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2),
+          "f"(c3));
 }
 template <bool BF16>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   if (BF16)
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   else
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// nibble pairs -> exact (q - 8) pairs, in the input dtype
+// ---------------------------------------------------------------------------------------------
+// nibble pairs -> f16/bf16 pairs.  Low nibbles sit at bits 0-3 / 16-19 of the word, high
+// nibbles at bits 4-7 / 20-23.
+// ---------------------------------------------------------------------------------------------
+// raw values (one LOP3 with the exponent pattern `mg` in a register): f16 (1024 + q) from low
+// nibbles, (1024 + 16 q) from high nibbles; bf16 (128 + q) from low nibbles only (bf16 has 7
+// mantissa bits).  mg = 0x64006400 (f16) or 0x43004300 (bf16).
+__device__ __forceinline__ uint32_t raw_lo(uint32_t w, uint32_t mg) {
+  return and_or<0x000F000Fu>(w, mg);
+}
+__device__ __forceinline__ uint32_t raw_hi_f16(uint32_t w, uint32_t mg) {
+  return and_or<0x00F000F0u>(w, mg);
+}
+// exact (q - 8) pairs
 template <bool BF16>
-__device__ __forceinline__ uint32_t nib_lo(uint32_t w) {
-  uint32_t x = (w & 0x000F000Fu) | (BF16 ? 0x43004300u : 0x64006400u);
+__device__ __forceinline__ uint32_t nib_lo(uint32_t w, uint32_t mg) {
+  uint32_t x = raw_lo(w, mg);
   if (BF16) {
-    const uint32_t c = 0x43084308u;
+    const uint32_t c = 0x43084308u;  // 136
     __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x),
                                *reinterpret_cast<const __nv_bfloat162*>(&c));
     return *reinterpret_cast<uint32_t*>(&r);
   } else {
-    const uint32_t c = 0x64086408u;
+    const uint32_t c = 0x64086408u;  // 1032
     __half2 r = __hsub2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<const __half2*>(&c));
     return *reinterpret_cast<uint32_t*>(&r);
   }
 }
 template <bool BF16>
-__device__ __forceinline__ uint32_t nib_hi(uint32_t w) {
+__device__ __forceinline__ uint32_t nib_hi(uint32_t w, uint32_t mg) {
   if (BF16) {
-    // bf16 has 7 mantissa bits: a high nibble at bits 4-7 would reach the exponent
-    return nib_lo<true>(w >> 4);
+    return nib_lo<true>(w >> 4, mg);
   } else {
-    uint32_t x = (w & 0x00F000F0u) | 0x64006400u;     // 1024 + 16 n
+    uint32_t x = raw_hi_f16(w, mg);                   // 1024 + 16 q
     const uint32_t s = 0x2C002C00u, c = 0xD480D480u;  // 1/16, -72
     __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<const __half2*>(&s),
                         *reinterpret_cast<const __half2*>(&c));
     return *reinterpret_cast<uint32_t*>(&r);
   }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float h2f(uint16_t bits) {
+  return BF16 ? __uint_as_float(static_cast<uint32_t>(bits) << 16)
+              : __half2float(__ushort_as_half(bits));
+}
+template <bool BF16>
+__device__ __forceinline__ uint16_t f2h(float v) {
+  return BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
+              : __half_as_ushort(__float2half_rn(v));
 }
 
 struct DecodeArgs {
@@ -126,6 +183,9 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs args) {
   using C = DCfg<D, Q4>;
+  constexpr int kSub = C::kSub;
+  constexpr int kTileKeys = C::kTileKeys;
+  constexpr int kNB = C::kNB;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -153,6 +213,7 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -162,8 +223,31 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
     }
     bool ok = true;
     int n = 0;
+    constexpr int kKeysPerLane = kTileKeys / 32;
     for (; n < ntiles; ++n) {
       const int s = n % C::kStages;
+      const int key0 = kb0 + n * kTileKeys;
+      // q4_0: this lane's scale rows (keys 4*lane .. 4*lane+3 of the tile), zero past Sk; the
+      // loads are issued before waiting for the slot so their latency overlaps the wait
+      uint32_t kr[kKeysPerLane][2], vr[kKeysPerLane][2];
+      if constexpr (Q4) {
+#pragma unroll
+        for (int j = 0; j < kKeysPerLane; ++j) {
+          const int key = key0 + kKeysPerLane * lane + j;
+          kr[j][0] = kr[j][1] = vr[j][0] = vr[j][1] = 0u;
+          if (key < args.Sk) {
+            const int64_t off = (bh * args.Sk + key) * C::kRow;
+            if (kNB == 4) {
+              const uint2 a = __ldg(reinterpret_cast<const uint2*>(args.k_scale + off));
+              const uint2 c = __ldg(reinterpret_cast<const uint2*>(args.v_scale + off));
+              kr[j][0] = a.x; kr[j][1] = a.y; vr[j][0] = c.x; vr[j][1] = c.y;
+            } else {
+              kr[j][0] = __ldg(reinterpret_cast<const uint32_t*>(args.k_scale + off));
+              vr[j][0] = __ldg(reinterpret_cast<const uint32_t*>(args.v_scale + off));
+            }
+          }
+        }
+      }
       if (n >= C::kStages) {
         if (lane == 0)
           ok = mbar_wait(bar_empty + 8 * s, ((n / C::kStages) - 1) & 1, abort_flag,
@@ -171,11 +255,10 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
       }
-      const int key0 = kb0 + n * kTileKeys;
       const uint32_t st = sbase + s * C::kStageBytes;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_full + 8 * s, 2 * C::kKBytes);
-        if (Q4) {
+        if constexpr (Q4) {
           tma_load_3d(st, &tm_k, bar_full + 8 * s, 0, key0, static_cast<int>(bh));
           tma_load_3d(st + C::kOffV, &tm_v, bar_full + 8 * s, 0, key0, static_cast<int>(bh));
         } else {
@@ -188,22 +271,57 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
           }
         }
       }
-      if (Q4) {
-        constexpr int kRow = (D / 32) * 2;  // scale bytes per key
-        for (int i = lane; i < 2 * kTileKeys; i += 32) {
-          const bool is_v = i >= kTileKeys;
-          const int r = is_v ? i - kTileKeys : i;
-          const int key = key0 + r;
-          const bool in = key < args.Sk;
-          const uint8_t* src =
-              (is_v ? args.v_scale : args.k_scale) + (bh * args.Sk + (in ? key : 0)) * kRow;
-          const uint32_t dst = st + (is_v ? C::kOffVs : C::kOffKs) + r * kRow;
-          if (kRow == 8)
-            cp_async_8(dst, src, in ? 8u : 0u);
+      if constexpr (Q4) {
+        uint8_t* stg = sgen + (st - sbase);
+#pragma unroll
+        for (int j = 0; j < kKeysPerLane; ++j) {
+          const int kt = kKeysPerLane * lane + j;  // key within the tile
+          float kf[kNB];
+#pragma unroll
+          for (int blk = 0; blk < kNB; ++blk)
+            kf[blk] = __half2float(__ushort_as_half(
+                          static_cast<uint16_t>(kr[j][blk >> 1] >> (16 * (blk & 1))))) *
+                      args.scale_log2;
+          float* kdst = reinterpret_cast<float*>(stg + C::kOffKs) + kt * kNB;
+          if (kNB == 4)
+            *reinterpret_cast<float4*>(kdst) = make_float4(kf[0], kf[1], kf[2], kf[3]);
           else
-            cp_async_4(dst, src, in ? 4u : 0u);
+            *reinterpret_cast<float2*>(kdst) = make_float2(kf[0], kf[1]);
+          if (BF16) {
+            float vf[kNB];
+#pragma unroll
+            for (int blk = 0; blk < kNB; ++blk)
+              vf[blk] = __half2float(__ushort_as_half(
+                  static_cast<uint16_t>(vr[j][blk >> 1] >> (16 * (blk & 1)))));
+            float* vdst = reinterpret_cast<float*>(stg + C::kOffVs) + kt * kNB;
+            if (kNB == 4)
+              *reinterpret_cast<float4*>(vdst) = make_float4(vf[0], vf[1], vf[2], vf[3]);
+            else
+              *reinterpret_cast<float2*>(vdst) = make_float2(vf[0], vf[1]);
+          }
         }
-        cp_async_mbar_arrive_noinc(bar_full + 8 * s);
+        if (!BF16) {
+          // key pairs (4*lane, 4*lane+1) and (4*lane+2, 4*lane+3): fp16 pairs per block at
+          // [16-key group][t][half][block], t and half from the pair's position in its group
+#pragma unroll
+          for (int pr = 0; pr < kKeysPerLane / 2; ++pr) {
+            const int ka = kKeysPerLane * lane + 2 * pr;  // even key of the pair
+            const int grp = ka >> 4, w16 = ka & 15;
+            const int h8 = w16 >> 3, t = (w16 & 7) >> 1;
+            uint32_t pv[kNB];
+#pragma unroll
+            for (int blk = 0; blk < kNB; ++blk)
+              pv[blk] = __byte_perm(vr[2 * pr][blk >> 1], vr[2 * pr + 1][blk >> 1],
+                                    (blk & 1) ? 0x7632u : 0x5410u);
+            uint32_t* vdst = reinterpret_cast<uint32_t*>(stg + C::kOffVs) +
+                             ((grp * 4 + t) * 2 + h8) * kNB;
+            if (kNB == 4)
+              *reinterpret_cast<uint4*>(vdst) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+            else
+              *reinterpret_cast<uint2*>(vdst) = make_uint2(pv[0], pv[1]);
+          }
+        }
+        mbar_arrive(bar_full + 8 * s);  // release: the scale stores above are visible
       }
     }
     if (!ok && lane == 0) {
@@ -215,38 +333,65 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
   }
 
   // -------------------------------------------------------------- consumers
-  const int cw = warp - 1;  // 0..3
+  const int cw = warp - 1;   // 0..3
   const int g8 = lane >> 2;  // fragment row group
   const int t4 = lane & 3;   // fragment column pair
   const float sl2 = args.scale_log2;
 
-  // Q^T as mma B fragments (k = head dim, n = query head of the group), loaded once.
-  // q4_0 uses a permutation of the head dimension that matches the nibble layout (see below).
+  // Q^T as mma B fragments (k = head dim, n = query head of the group), loaded once.  For q4_0
+  // the head dimension is permuted to match the nibble layout: k-step (block, half) uses
+  // fragment column 2t+e <-> element 32 block + 16 half + 4t + 2e and column 2t+8+e <->
+  // 32 block + 16 half + 4t + 1 + 2e; the high-nibble k-steps of f16 take Q / 16 (exact) to
+  // cancel the factor 16 of the raw (1024 + 16 q) values.
   uint32_t qf[D / 16][2];
+  // q4_0: -(offset * sum of Q) per block and head, the accumulator start that removes the raw
+  // values' constant offsets (f16: 1032 on low halves, 72 on high halves; bf16: 136)
+  float corr[kNB][2];
   {
     const int hq = hkv * G + g8;
     const uint16_t* qrow = args.q + (static_cast<int64_t>(b) * args.Hq + hq) * D;
     const bool valid = g8 < G;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      int d0, d1, d2, d3;
+      int d[4];
       if (Q4) {
-        // k-step kk = (block kk/2, nibble half kk%2): fragment column 2t+e <-> element
-        // 16*kk + 4t + 2e, column 2t+8+e <-> element 16*kk + 4t + 1 + 2e
-        d0 = 16 * kk + 4 * t4;
-        d1 = d0 + 2;
-        d2 = d0 + 1;
-        d3 = d0 + 3;
+        d[0] = 16 * kk + 4 * t4;
+        d[1] = d[0] + 2;
+        d[2] = d[0] + 1;
+        d[3] = d[0] + 3;
       } else {
-        d0 = 16 * kk + 2 * t4;
-        d1 = d0 + 1;
-        d2 = d0 + 8;
-        d3 = d0 + 9;
+        d[0] = 16 * kk + 2 * t4;
+        d[1] = d[0] + 1;
+        d[2] = d[0] + 8;
+        d[3] = d[0] + 9;
       }
-      const uint32_t e0 = valid ? qrow[d0] : 0u, e1 = valid ? qrow[d1] : 0u;
-      const uint32_t e2 = valid ? qrow[d2] : 0u, e3 = valid ? qrow[d3] : 0u;
-      qf[kk][0] = e0 | (e1 << 16);
-      qf[kk][1] = e2 | (e3 << 16);
+      uint32_t e[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint16_t v = valid ? qrow[d[i]] : static_cast<uint16_t>(0);
+        if (Q4 && !BF16 && (kk & 1)) v = f2h<false>(h2f<false>(v) * 0.0625f);
+        e[i] = v;
+      }
+      qf[kk][0] = e[0] | (e[1] << 16);
+      qf[kk][1] = e[2] | (e[3] << 16);
+    }
+    if constexpr (Q4) {
+#pragma unroll
+      for (int blk = 0; blk < kNB; ++blk) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h2 = hkv * G + 2 * t4 + hh;
+          float lo = 0.f, hi = 0.f;
+          if (2 * t4 + hh < G) {
+            const uint16_t* qr = args.q + (static_cast<int64_t>(b) * args.Hq + h2) * D + 32 * blk;
+            for (int i = 0; i < 16; ++i) {
+              lo += h2f<BF16>(qr[i]);
+              hi += h2f<BF16>(qr[16 + i]);
+            }
+          }
+          corr[blk][hh] = BF16 ? -136.f * (lo + hi) : -(1032.f * lo + 72.f * hi);
+        }
+      }
     }
   }
 
@@ -256,74 +401,108 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
   for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY;  // running max (base-2 scaled) for heads 2t, 2t+1
   float l0 = 0.f, l1 = 0.f;              // this thread's share of the row sums
+  const int mi = lane >> 3, r8 = lane & 7;  // ldmatrix: matrix index and row of this lane
+  const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
 
   bool ok = true;
   for (int n = 0; n < ntiles; ++n) {
     const int s = n % C::kStages;
-    if (lane == 0)
-      ok = mbar_wait(bar_full + 8 * s, (n / C::kStages) & 1, abort_flag, &g_decode_error);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (!ok) break;
+    ok = mbar_wait(bar_full + 8 * s, (n / C::kStages) & 1, abort_flag, &g_decode_error);
+    if (!__all_sync(0xffffffffu, ok)) break;
     const uint32_t st = sbase + s * C::kStageBytes;
-    const int kl = 16 * cw;                        // this warp's first key in the tile
-    const int keyg = kb0 + n * kTileKeys + kl + g8; // absolute key of fragment row g
-    // ---------------- S^T = K Q^T (16 keys x 8 heads)
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (Q4) {
-      const __half* ks = reinterpret_cast<const __half*>(sgen + (st - sbase) + C::kOffKs);
-      const int mi = lane >> 3, r = lane & 7;
+    const int tile_key0 = kb0 + n * kTileKeys;
+
+    // ---------------- S^T = K Q^T, kSub sub-tiles of 16 keys x 8 heads
+    float sc[kSub][4];
 #pragma unroll
-      for (int bb = 0; bb < D / 32; bb += 2) {
-        const int key = kl + (mi & 1) * 8 + r;
-        const int blk = bb + (mi >> 1);
-        const int chunk = (D == 128) ? (blk ^ ((key >> 1) & 3)) : (blk ^ ((key >> 2) & 1));
-        uint32_t w[4];
-        ldsm_x4(st + key * (D / 2) + chunk * 16, w[0], w[1], w[2], w[3]);
+    for (int u = 0; u < kSub; ++u) {
+      const int kl = (kSub * 16) * cw + 16 * u;  // first key of the sub-tile in the stage
+      sc[u][0] = sc[u][1] = sc[u][2] = sc[u][3] = 0.f;
+      if constexpr (Q4) {
+        float kf_g[4], kf_g8[4];  // f32 scales (times the base-2 softmax scale), keys g, g+8
+        if (kNB == 4) {
+          const uint4 x = lds128(st + C::kOffKs + (kl + g8) * 16);
+          const uint4 y = lds128(st + C::kOffKs + (kl + g8 + 8) * 16);
+          kf_g[0] = __uint_as_float(x.x); kf_g[1] = __uint_as_float(x.y);
+          kf_g[2] = __uint_as_float(x.z); kf_g[3] = __uint_as_float(x.w);
+          kf_g8[0] = __uint_as_float(y.x); kf_g8[1] = __uint_as_float(y.y);
+          kf_g8[2] = __uint_as_float(y.z); kf_g8[3] = __uint_as_float(y.w);
+        } else {
+          const uint2 x = lds64(st + C::kOffKs + (kl + g8) * 8);
+          const uint2 y = lds64(st + C::kOffKs + (kl + g8 + 8) * 8);
+          kf_g[0] = __uint_as_float(x.x); kf_g[1] = __uint_as_float(x.y);
+          kf_g8[0] = __uint_as_float(y.x); kf_g8[1] = __uint_as_float(y.y);
+          kf_g[2] = kf_g[3] = kf_g8[2] = kf_g8[3] = 0.f;
+        }
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int blkk = bb + e;
-          const uint32_t wg = w[2 * e], wg8 = w[2 * e + 1];
-          float cb[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816<BF16>(cb, nib_lo<BF16>(wg), nib_lo<BF16>(wg8), nib_lo<BF16>(wg >> 8),
-                         nib_lo<BF16>(wg8 >> 8), qf[2 * blkk][0], qf[2 * blkk][1]);
-          mma16816<BF16>(cb, nib_hi<BF16>(wg), nib_hi<BF16>(wg8), nib_hi<BF16>(wg >> 8),
-                         nib_hi<BF16>(wg8 >> 8), qf[2 * blkk + 1][0], qf[2 * blkk + 1][1]);
-          const float dg = __half2float(ks[(kl + g8) * (D / 32) + blkk]);
-          const float dg8 = __half2float(ks[(kl + g8 + 8) * (D / 32) + blkk]);
-          sc[0] = fmaf(cb[0], dg, sc[0]);
-          sc[1] = fmaf(cb[1], dg, sc[1]);
-          sc[2] = fmaf(cb[2], dg8, sc[2]);
-          sc[3] = fmaf(cb[3], dg8, sc[3]);
+        for (int bb = 0; bb < kNB; bb += 2) {
+          const int key = kl + (mi & 1) * 8 + r8;
+          const int blk = bb + (mi >> 1);
+          const int chunk = (D == 128) ? (blk ^ ((key >> 1) & 3)) : (blk ^ ((key >> 2) & 1));
+          uint32_t w[4];
+          ldsm_x4(st + key * (D / 2) + chunk * 16, w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int blkk = bb + e;
+            const uint32_t wg = w[2 * e], wg8 = w[2 * e + 1];
+            const uint32_t wgs = wg >> 8, wg8s = wg8 >> 8;
+            float cb[4];
+            mma16816_c<BF16>(cb, raw_lo(wg, mg), raw_lo(wg8, mg), raw_lo(wgs, mg),
+                             raw_lo(wg8s, mg), qf[2 * blkk][0], qf[2 * blkk][1], corr[blkk][0],
+                             corr[blkk][1], corr[blkk][0], corr[blkk][1]);
+            if (BF16)
+              mma16816<BF16>(cb, raw_lo(wg >> 4, mg), raw_lo(wg8 >> 4, mg),
+                             raw_lo(wgs >> 4, mg), raw_lo(wg8s >> 4, mg),
+                             qf[2 * blkk + 1][0], qf[2 * blkk + 1][1]);
+            else
+              mma16816<BF16>(cb, raw_hi_f16(wg, mg), raw_hi_f16(wg8, mg), raw_hi_f16(wgs, mg),
+                             raw_hi_f16(wg8s, mg), qf[2 * blkk + 1][0], qf[2 * blkk + 1][1]);
+            const float dg = kf_g[blkk], dg8 = kf_g8[blkk];
+            sc[u][0] = fmaf(cb[0], dg, sc[u][0]);
+            sc[u][1] = fmaf(cb[1], dg, sc[u][1]);
+            sc[u][2] = fmaf(cb[2], dg8, sc[u][2]);
+            sc[u][3] = fmaf(cb[3], dg8, sc[u][3]);
+          }
+        }
+      } else {
+        const int key = kl + (mi & 1) * 8 + r8;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int d0 = 16 * kk + (mi >> 1) * 8;
+          const uint32_t addr = st + (d0 >> 6) * (kTileKeys * 128) + key * 128 +
+                                ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(addr, a0, a1, a2, a3);
+          mma16816<BF16>(sc[u], a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
         }
       }
-    } else {
-      const int mi = lane >> 3, r = lane & 7;
-      const int key = kl + (mi & 1) * 8 + r;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int d0 = 16 * kk + (mi >> 1) * 8;
-        const uint32_t addr =
-            st + (d0 >> 6) * (kTileKeys * 128) + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(addr, a0, a1, a2, a3);
-        mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-      }
     }
-    // ---------------- online softmax over this warp's 16 keys
-    const bool vg = keyg < kb1, vg8 = keyg + 8 < kb1;
-    const float t0 = vg ? sc[0] * sl2 : -INFINITY;
-    const float t1 = vg ? sc[1] * sl2 : -INFINITY;
-    const float t2 = vg8 ? sc[2] * sl2 : -INFINITY;
-    const float t3 = vg8 ? sc[3] * sl2 : -INFINITY;
-    float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+
+    // ---------------- online softmax over this warp's kSub * 16 keys
+    // scores in base-2 units (the q4_0 K scales already carry the softmax scale); keys past
+    // the split's end are masked, which only the last tile of a split can contain
+    float t[kSub][4];
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+    const bool full_tile = tile_key0 + kTileKeys <= kb1;
+#pragma unroll
+    for (int u = 0; u < kSub; ++u) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) t[u][i] = Q4 ? sc[u][i] : sc[u][i] * sl2;
+      if (!full_tile) {
+        const int keyg = tile_key0 + (kSub * 16) * cw + 16 * u + g8;
+        if (keyg >= kb1) t[u][0] = t[u][1] = -INFINITY;
+        if (keyg + 8 >= kb1) t[u][2] = t[u][3] = -INFINITY;
+      }
+      mx0 = fmaxf(mx0, fmaxf(t[u][0], t[u][2]));
+      mx1 = fmaxf(mx1, fmaxf(t[u][1], t[u][3]));
+    }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
-    const bool grow = (nm0 > m0) || (nm1 > m1);
-    if (__any_sync(0xffffffffu, grow)) {
+    if (__any_sync(0xffffffffu, (nm0 > m0) || (nm1 > m1))) {
       const float a0 = (nm0 == -INFINITY) ? 1.f : ex2(m0 - nm0);
       const float a1 = (nm1 == -INFINITY) ? 1.f : ex2(m1 - nm1);
       l0 *= a0;
@@ -339,52 +518,104 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
       m1 = nm1;
     }
     const float b0 = (m0 == -INFINITY) ? 0.f : m0, b1 = (m1 == -INFINITY) ? 0.f : m1;
-    const float p0 = ex2(t0 - b0), p1 = ex2(t1 - b1), p2 = ex2(t2 - b0), p3 = ex2(t3 - b1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
+    float p[kSub][4];
+#pragma unroll
+    for (int u = 0; u < kSub; ++u) {
+      p[u][0] = ex2(t[u][0] - b0);
+      p[u][1] = ex2(t[u][1] - b1);
+      p[u][2] = ex2(t[u][2] - b0);
+      p[u][3] = ex2(t[u][3] - b1);
+      l0 += p[u][0] + p[u][2];
+      l1 += p[u][1] + p[u][3];
+    }
+
     // ---------------- O^T += V^T P^T
-    if (Q4) {
-      const __half* vs = reinterpret_cast<const __half*>(sgen + (st - sbase) + C::kOffVs);
-      const int mi = lane >> 3, r = lane & 7;
-      const uint32_t vbase = st + C::kOffV;
 #pragma unroll
-      for (int bb = 0; bb < D / 32; bb += 2) {
-        const int key = kl + (mi & 1) * 8 + r;
-        const int blk = bb + (mi >> 1);
-        const int chunk = (D == 128) ? (blk ^ ((key >> 1) & 3)) : (blk ^ ((key >> 2) & 1));
-        uint32_t w[4];
-        ldsm_x4_t(vbase + key * (D / 2) + chunk * 16, w[0], w[1], w[2], w[3]);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int blkk = bb + e;
-          const float dg = __half2float(vs[(kl + g8) * (D / 32) + blkk]);
-          const float dg8 = __half2float(vs[(kl + g8 + 8) * (D / 32) + blkk]);
-          // P scaled by this block's V scale, transposed into the B fragment (keys x heads)
-          const uint32_t pb0 = movtrans(pack2<BF16>(p0 * dg, p1 * dg));
-          const uint32_t pb1 = movtrans(pack2<BF16>(p2 * dg8, p3 * dg8));
-          const uint32_t w1 = w[2 * e], w2 = w[2 * e + 1];
-          // m-tile (block, low nibbles): rows g <-> element 2g, g+8 <-> element 2g+1
-          mma16816<BF16>(o[2 * blkk], nib_lo<BF16>(w1), nib_lo<BF16>(w1 >> 8), nib_lo<BF16>(w2),
-                         nib_lo<BF16>(w2 >> 8), pb0, pb1);
-          // m-tile (block, high nibbles): rows g <-> element 16+2g, g+8 <-> element 17+2g
-          mma16816<BF16>(o[2 * blkk + 1], nib_hi<BF16>(w1), nib_hi<BF16>(w1 >> 8),
-                         nib_hi<BF16>(w2), nib_hi<BF16>(w2 >> 8), pb0, pb1);
+    for (int u = 0; u < kSub; ++u) {
+      const int kl = (kSub * 16) * cw + 16 * u;
+      if constexpr (Q4) {
+        const uint32_t vbase = st + C::kOffV;
+        // P of keys (2t, 2t+1) and (2t+8, 2t+9) for head g (f16: transposed once, then scaled
+        // per block with the V scales of those key pairs)
+        uint32_t pt0 = 0, pt1 = 0;
+        uint32_t sp01[4] = {0u, 0u, 0u, 0u};  // fp16 V-scale pairs of keys (2t, 2t+1), per block
+        uint32_t sp89[4] = {0u, 0u, 0u, 0u};  // and of keys (2t+8, 2t+9)
+        float vf_g[4] = {0.f, 0.f, 0.f, 0.f}, vf_g8[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (!BF16) {
+          pt0 = movtrans(pack2<false>(p[u][0], p[u][1]));
+          pt1 = movtrans(pack2<false>(p[u][2], p[u][3]));
+          const uint32_t pa = st + C::kOffVs + ((kl >> 4) * 4 + t4) * 2 * kNB * 4;
+          if (kNB == 4) {
+            const uint4 x = lds128(pa), y = lds128(pa + 16);
+            sp01[0] = x.x; sp01[1] = x.y; sp01[2] = x.z; sp01[3] = x.w;
+            sp89[0] = y.x; sp89[1] = y.y; sp89[2] = y.z; sp89[3] = y.w;
+          } else {
+            const uint2 x = lds64(pa), y = lds64(pa + 8);
+            sp01[0] = x.x; sp01[1] = x.y; sp89[0] = y.x; sp89[1] = y.y;
+          }
+        } else {
+          if (kNB == 4) {
+            const uint4 x = lds128(st + C::kOffVs + (kl + g8) * 16);
+            const uint4 y = lds128(st + C::kOffVs + (kl + g8 + 8) * 16);
+            vf_g[0] = __uint_as_float(x.x); vf_g[1] = __uint_as_float(x.y);
+            vf_g[2] = __uint_as_float(x.z); vf_g[3] = __uint_as_float(x.w);
+            vf_g8[0] = __uint_as_float(y.x); vf_g8[1] = __uint_as_float(y.y);
+            vf_g8[2] = __uint_as_float(y.z); vf_g8[3] = __uint_as_float(y.w);
+          } else {
+            const uint2 x = lds64(st + C::kOffVs + (kl + g8) * 8);
+            const uint2 y = lds64(st + C::kOffVs + (kl + g8 + 8) * 8);
+            vf_g[0] = __uint_as_float(x.x); vf_g[1] = __uint_as_float(x.y);
+            vf_g8[0] = __uint_as_float(y.x); vf_g8[1] = __uint_as_float(y.y);
+          }
         }
-      }
-    } else {
-      const uint32_t pb0 = movtrans(pack2<BF16>(p0, p1));
-      const uint32_t pb1 = movtrans(pack2<BF16>(p2, p3));
-      const int mi = lane >> 3, r = lane & 7;
-      const int key = kl + (mi >> 1) * 8 + r;
-      const uint32_t vbase = st + C::kOffV;
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        const int d0 = 16 * mt + (mi & 1) * 8;
-        const uint32_t addr = vbase + (d0 >> 6) * (kTileKeys * 128) + key * 128 +
-                              ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(addr, a0, a1, a2, a3);
-        mma16816<BF16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+        for (int bb = 0; bb < kNB; bb += 2) {
+          const int key = kl + (mi & 1) * 8 + r8;
+          const int blk = bb + (mi >> 1);
+          const int chunk = (D == 128) ? (blk ^ ((key >> 1) & 3)) : (blk ^ ((key >> 2) & 1));
+          uint32_t w[4];
+          ldsm_x4_t(vbase + key * (D / 2) + chunk * 16, w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int blkk = bb + e;
+            uint32_t pb0, pb1;
+            if constexpr (!BF16) {
+              __half2 r0 = __hmul2(*reinterpret_cast<const __half2*>(&pt0),
+                                   *reinterpret_cast<const __half2*>(&sp01[blkk]));
+              __half2 r1 = __hmul2(*reinterpret_cast<const __half2*>(&pt1),
+                                   *reinterpret_cast<const __half2*>(&sp89[blkk]));
+              pb0 = *reinterpret_cast<uint32_t*>(&r0);
+              pb1 = *reinterpret_cast<uint32_t*>(&r1);
+            } else {
+              // bf16: scale P in f32 (the fp16 scale is exact there), then round once
+              const float dg = vf_g[blkk], dg8 = vf_g8[blkk];
+              pb0 = movtrans(pack2<true>(p[u][0] * dg, p[u][1] * dg));
+              pb1 = movtrans(pack2<true>(p[u][2] * dg8, p[u][3] * dg8));
+            }
+            const uint32_t w1 = w[2 * e], w2 = w[2 * e + 1];
+            // m-tile (block, low nibbles): rows g <-> element 2g, g+8 <-> element 2g+1
+            const uint32_t w1s = w1 >> 8, w2s = w2 >> 8;
+            mma16816<BF16>(o[2 * blkk], nib_lo<BF16>(w1, mg), nib_lo<BF16>(w1s, mg),
+                           nib_lo<BF16>(w2, mg), nib_lo<BF16>(w2s, mg), pb0, pb1);
+            // m-tile (block, high nibbles): rows g <-> element 16+2g, g+8 <-> element 17+2g
+            mma16816<BF16>(o[2 * blkk + 1], nib_hi<BF16>(w1, mg), nib_hi<BF16>(w1s, mg),
+                           nib_hi<BF16>(w2, mg), nib_hi<BF16>(w2s, mg), pb0, pb1);
+          }
+        }
+      } else {
+        const uint32_t pb0 = movtrans(pack2<BF16>(p[u][0], p[u][1]));
+        const uint32_t pb1 = movtrans(pack2<BF16>(p[u][2], p[u][3]));
+        const int key = kl + (mi >> 1) * 8 + r8;
+        const uint32_t vbase = st + C::kOffV;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d0 = 16 * mt + (mi & 1) * 8;
+          const uint32_t addr = vbase + (d0 >> 6) * (kTileKeys * 128) + key * 128 +
+                                ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(addr, a0, a1, a2, a3);
+          mma16816<BF16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
       }
     }
     __syncwarp();
@@ -392,7 +623,6 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
   }
 
   // ------------------------------------------------------------------ merge the 4 warps
-  // full row sums of this warp's keys
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -454,45 +684,74 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
   }
 }
 
+constexpr int kMaxCombineSplits = 1024;
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const float* __restrict__ partial,
+__global__ void __launch_bounds__(128) decode_combine_kernel(const float* partial,
                                                              uint16_t* __restrict__ o, int nsplit) {
   constexpr int kStride = D + 4;
+  __shared__ float wsm[kMaxCombineSplits];  // e^(m_s - M) per split
+  __shared__ float red[2][4];
   const int64_t row = blockIdx.x;  // b * Hq + hq
   const float* p = partial + row * nsplit * kStride;
+  pdl_wait_primary();  // the split kernel's partials are complete and visible
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // M = max m_s
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p[s * kStride]);
+  for (int s = tid; s < nsplit; s += blockDim.x) M = fmaxf(M, p[s * kStride]);
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red[0][warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
+  // weights and L = sum e^(m_s - M) l_s
   float L = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
+  for (int s = tid; s < nsplit; s += blockDim.x) {
     const float ms = p[s * kStride];
-    if (ms != -INFINITY) L += ex2(ms - M) * p[s * kStride + 1];
+    const float wgt = (ms == -INFINITY) ? 0.f : ex2(ms - M);
+    wsm[s] = wgt;
+    L += wgt * p[s * kStride + 1];
   }
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float ms = p[s * kStride];
-      if (ms != -INFINITY) acc += ex2(ms - M) * p[s * kStride + 4 + d];
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  if (lane == 0) red[1][warp] = L;
+  __syncthreads();
+  L = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+  const float inv = 1.f / L;
+  for (int d = tid; d < D; d += blockDim.x) {
+    // eight independent loads in flight per thread
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int s = 0;
+    for (; s + 8 <= nsplit; s += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = p[(s + j) * kStride + 4 + d];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(wsm[s + j], v[j], acc[j]);
     }
-    const float v = acc / L;
-    o[row * D + d] = BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
-                          : __half_as_ushort(__float2half_rn(v));
+    for (; s < nsplit; ++s) acc[0] = fmaf(wsm[s], p[s * kStride + 4 + d], acc[0]);
+    const float tot = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    o[row * D + d] = f2h<BF16>(tot * inv);
   }
 }
 
 }  // namespace
 
-void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, int* nsplit, int* chunk) {
-  // one wave of CTAs at the resident count of the q4_0 configuration, equal key chunks
+int decode_tile_keys(bool q4) {
+  return q4 ? DCfg<128, true>::kTileKeys : DCfg<128, false>::kTileKeys;
+}
+
+void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool q4, int* nsplit, int* chunk) {
+  // one wave of CTAs at the kernel's resident count, equal key chunks of whole tiles
+  const int tile = decode_tile_keys(q4);
   const int units = B * Hkv;
-  const int slots = num_sms * 4;
-  int ns = (slots + units / 2) / units;
+  const int slots = num_sms * (q4 ? DCfg<128, true>::kCtasPerSm : DCfg<128, false>::kCtasPerSm);
+  int ns = slots / units;
   if (ns < 1) ns = 1;
-  const int max_tiles = (Sk_eff + kTileKeys - 1) / kTileKeys;
+  const int max_tiles = (Sk_eff + tile - 1) / tile;
   if (ns > max_tiles) ns = max_tiles;
+  if (ns > kMaxCombineSplits) ns = kMaxCombineSplits;
   if (ns < 1) ns = 1;
   int ck = (Sk_eff + ns - 1) / ns;
-  ck = (ck + kTileKeys - 1) / kTileKeys * kTileKeys;
-  if (ck < kTileKeys) ck = kTileKeys;
+  ck = (ck + tile - 1) / tile * tile;
   *chunk = ck;
   *nsplit = (Sk_eff + ck - 1) / ck;
 }
@@ -520,8 +779,22 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D, BF16><<<L.B * L.Hq, 128, 0, stream>>>(
-      L.partial, static_cast<uint16_t*>(L.o), L.nsplit);
+  // the combine kernel is a programmatic dependent of the split kernel: it is scheduled while
+  // the split kernel runs and waits (griddepcontrol.wait) for its partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.B * L.Hq);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16>,
+                         static_cast<const float*>(L.partial), static_cast<uint16_t*>(L.o),
+                         L.nsplit);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

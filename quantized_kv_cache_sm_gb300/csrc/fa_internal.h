@@ -26,15 +26,17 @@ struct DecodeLaunch {
   void* o;
   const void* k_scale;           // q4_0 only
   const void* v_scale;
-  float* partial;                // [B, Hkv, nsplit, G, D + 2] f32 (workspace)
+  float* partial;                // [B, Hq, nsplit, D + 4] f32: m, l, pad, pad, O (workspace)
   int B, Hq, Hkv, Sk_eff, Sk, D, nsplit, chunk;
   float scale;
   bool bf16, q4;
 };
 cudaError_t decode_launch(const DecodeLaunch& L, cudaStream_t stream);
 uint32_t decode_take_error();
-// decode work split for a given shape (shared by the workspace query and the launch)
-void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, int* nsplit, int* chunk);
+// decode work split for a given shape and cache format (shared by the workspace query and the
+// launch), and the keys per pipeline stage (the TMA box height)
+void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool q4, int* nsplit, int* chunk);
+int decode_tile_keys(bool q4);
 
 cudaError_t quantize_launch(const void* x, void* nib, void* scale, int64_t rows, int D, bool bf16,
                             cudaStream_t stream);

@@ -67,8 +67,9 @@ enum {
   kBarSFull1 = 2,
   kBarPReady0 = 3,
   kBarPReady1 = 4,
-  kBarODone = 5,
-  kBarDrain = 6,
+  kBarODone0 = 5,     // PV(j) commits alternate between two barriers so that a waiter is
+  kBarDrain = 6,      // never two phases behind (parity waits alias two phases apart)
+  kBarODone1 = 7,
   kBarRingFull = 8,    // + stage   (up to 8 stages)
   kBarRingEmpty = 16,  // + stage
   kBarRawFull = 24,    // + raw stage
@@ -94,15 +95,15 @@ template <bool BF16>
 struct Dq;
 template <>
 struct Dq<false> {
-  // low nibbles at bits 0-3 / 16-19 -> (n - 8) exactly
-  static __device__ __forceinline__ __half2 lo(uint32_t w) {
-    uint32_t x = (w & 0x000F000Fu) | 0x64006400u;  // 1024 + n
+  // low nibbles at bits 0-3 / 16-19 -> (n - 8) exactly; mg = 0x64006400 in a register
+  static __device__ __forceinline__ __half2 lo(uint32_t w, uint32_t mg) {
+    uint32_t x = and_or<0x000F000Fu>(w, mg);  // 1024 + n
     return __hsub2(*reinterpret_cast<__half2*>(&x), __halves2half2(__ushort_as_half(0x6408),
                                                                     __ushort_as_half(0x6408)));
   }
   // high nibbles at bits 4-7 / 20-23 -> (n - 8) exactly
-  static __device__ __forceinline__ __half2 hi(uint32_t w) {
-    uint32_t x = (w & 0x00F000F0u) | 0x64006400u;  // 1024 + 16 n
+  static __device__ __forceinline__ __half2 hi(uint32_t w, uint32_t mg) {
+    uint32_t x = and_or<0x00F000F0u>(w, mg);  // 1024 + 16 n
     const __half2 s = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
     const __half2 c = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));  // -72
     return __hfma2(*reinterpret_cast<__half2*>(&x), s, c);
@@ -114,15 +115,17 @@ struct Dq<false> {
 };
 template <>
 struct Dq<true> {
-  static __device__ __forceinline__ __nv_bfloat162 lo(uint32_t w) {
-    uint32_t x = (w & 0x000F000Fu) | 0x43004300u;  // 128 + n
+  static __device__ __forceinline__ __nv_bfloat162 lo(uint32_t w, uint32_t mg) {
+    uint32_t x = and_or<0x000F000Fu>(w, mg);  // 128 + n (mg = 0x43004300)
     const uint32_t c = 0x43084308u;                 // 136
     return __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x),
                    *reinterpret_cast<const __nv_bfloat162*>(&c));
   }
   // bf16 has 7 mantissa bits, so a high nibble at bits 4-7 would reach the exponent: shift it
   // down to bits 0-3 first
-  static __device__ __forceinline__ __nv_bfloat162 hi(uint32_t w) { return lo(w >> 4); }
+  static __device__ __forceinline__ __nv_bfloat162 hi(uint32_t w, uint32_t mg) {
+    return lo(w >> 4, mg);
+  }
   static __device__ __forceinline__ uint32_t scale(__nv_bfloat162 v, float d) {
     // (n - 8) * d rounded once to bf16: the product of a 4-bit integer and an fp16 value is
     // exact in f32, so round only after the f32 multiply.
@@ -165,7 +168,8 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
     mbar_init(bar(kBarSFull1), 1);
     mbar_init(bar(kBarPReady0), 128);
     mbar_init(bar(kBarPReady1), 128);
-    mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarODone0), 1);
+    mbar_init(bar(kBarODone1), 1);
     mbar_init(bar(kBarDrain), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(kBarRingFull + s), Q4 ? 128 : 1);
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
           mma_ts(tmem + kColO, pcol + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
         release(s);
-        mma_commit(bar(kBarODone));
+        mma_commit(bar((j & 1) ? kBarODone1 : kBarODone0));
       };
       if (ok) issue_qk(0);
       if (ok && nb > 1) issue_qk(1);
@@ -359,6 +363,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
         for (int c = 0; c < kBN / 32; ++c) {
           tmem_ld32(tmem + lane_off + scol + 32 * c, r);
           tmem_wait_ld();
+          reg_fence32(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
         }
@@ -386,7 +391,8 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
         }
         if (j > 0) {
           // O holds the blocks before j; PV(j-1) must have landed before it is rescaled
-          ok = mbar_wait(bar(kBarODone), (j - 1) & 1, abort_flag, &g_prefill_error);
+          ok = mbar_wait(bar(((j - 1) & 1) ? kBarODone1 : kBarODone0), ((j - 1) >> 1) & 1,
+                         abort_flag, &g_prefill_error);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
@@ -402,6 +408,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
           tmem_wait_st();
         }
       }
+      // P = 2^(t - f) packed in pairs over S
       const float nf = -f;
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) {
@@ -420,7 +427,9 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
       mbar_arrive(bar((j & 1) ? kBarPReady1 : kBarPReady0));
     }
     if (ok) {
-      ok = mbar_wait(bar(kBarODone), (nb - 1) & 1, abort_flag, &g_prefill_error);
+      // PV(nb-1) done implies every earlier MMA is done (one commit tracks all of them)
+      ok = mbar_wait(bar(((nb - 1) & 1) ? kBarODone1 : kBarODone0), ((nb - 1) >> 1) & 1,
+                     abort_flag, &g_prefill_error);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -453,6 +462,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
     // ---------------------------------------------------------------- q4_0 dequant
     // thread t expands key row t of each raw tile into the 128B-swizzled f16/bf16 ring stage
     const int t = threadIdx.x - 6 * 32;
+    const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
     bool ok = true;
     const int ntiles = 2 * nb;
     for (int n = 0; n < ntiles; ++n) {
@@ -483,15 +493,15 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
           const uint32_t c2 = __byte_perm(w[q], 0u, 0x5352); // byte2 at b0, byte3 at b2
           if (BF16) {
             const float d = __half2float(dh);
-            outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a), d);
-            outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2), d);
-            outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a), d);
-            outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2), d);
+            outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a, mg), d);
+            outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2, mg), d);
+            outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a, mg), d);
+            outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2, mg), d);
           } else {
-            outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a), dh);
-            outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2), dh);
-            outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a), dh);
-            outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2), dh);
+            outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a, mg), dh);
+            outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2, mg), dh);
+            outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a, mg), dh);
+            outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2, mg), dh);
           }
         }
         // elements 32 blk + 8 cc .. +7 form 16-byte chunk (4 blk + cc) of the row
