@@ -40,6 +40,7 @@ struct DCfg {
   static constexpr int kTileKeys = 16 * kSub * kConsumers;     // keys per stage
   static constexpr int kNB = D / 32;                           // q4_0 blocks per key row
   static constexpr int kRow = kNB * 2;                         // scale bytes per key row
+  static_assert(kRow > 0, "scale row");
   static constexpr int kNibBytes = kTileKeys * D / 2;
   // scales as the producer leaves them: K as f32 [key][block] (times the softmax scale in base
   // 2); V as f32 [key][block] (bf16) or as fp16 key pairs [16-key group][t][half][block] (f16)

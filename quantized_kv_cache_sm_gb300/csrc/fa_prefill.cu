@@ -6,24 +6,30 @@
 // This is the fused kernel of "perf(rocm): defer SDPA accumulator rescale, stage Q once per
 // block (#2306)" (Conversation; What changed), rebuilt for tcgen05:
 //
-//  * one CTA owns 128 query rows of one query head; Q is brought into shared memory once by TMA
-//    and stays there for the CTA's whole key range ("Q is staged once per block");
+//  * one CTA owns two 128-row query tiles (A, B) of one query head; both Q tiles are brought
+//    into shared memory once by TMA and stay there for the CTA's whole key range ("Q is staged
+//    once per block");
 //  * K and V tiles of 128 keys stream through a ring of shared-memory stages, either by TMA
 //    (dense f16/bf16 cache) or as q4_0 nibble/scale tiles that dequant warps expand into the same
 //    f16/bf16 swizzled layout (the fused K and V dequant of "FlashAttention on gfx90a: Why It's
-//    Broken and How to Fix It", Why FA-off Can't Do V Quantization, point 5);
-//  * S = Q K^T and O += P V are tcgen05.mma into tensor memory (S double-buffered, O resident);
+//    Broken and How to Fix It", Why FA-off Can't Do V Quantization, point 5); every K/V tile
+//    serves both query tiles;
+//  * S = Q K^T and O += P V are tcgen05.mma into tensor memory; the single MMA thread
+//    interleaves the tiles (PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1)) so the tensor core works on
+//    one tile while the softmax warps of the other run;
 //  * the softmax warps own one row each: block max, the deferred rescale, P = 2^(t - f) written
 //    back over S as f16/bf16 for the PV MMA, running row sum l;
 //  * deferred rescale (#2306, kFaWmmaRescaleMargin): a row keeps its frame f until a block max
 //    exceeds f by more than 10 natural-log units; only then are O and l multiplied by
 //    e^(f_old - f_new).  P stays below e^10 = 22026 in every frame.
 //
-// Warp roles (dense: 6 warps; q4_0: 10 warps):
-//   warp 0      TMA producer (one lane)
-//   warp 1      TMEM allocator + MMA issuer (one lane)
-//   warps 2..5  softmax / rescale / epilogue, one query row per thread
-//   warps 6..9  q4_0 dequant (q4_0 variant only), one key row per thread
+// Warp roles (dense: 12 warps; q4_0: 16 warps):
+//   warp 0       TMA producer (one lane)
+//   warp 1       TMEM allocator + MMA issuer (one lane)
+//   warps 2, 3   idle
+//   warps 4..7   softmax / rescale / epilogue of query tile A, one row per thread
+//   warps 8..11  the same for query tile B
+//   warps 12..15 q4_0 dequant (q4_0 variant only), one key row per thread
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -33,44 +39,43 @@ __device__ uint32_t g_prefill_error;
 
 namespace {
 
-constexpr int kBM = 128;                      // query rows per CTA
+constexpr int kBM = 128;                      // query rows per tile
 constexpr int kBN = 128;                      // keys per tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMarginLog2 = 10.0f * kLog2e; // the 10-point margin, in base-2 units
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// TMEM column of the S block of query tile t (0: A, 1: B); P overwrites its first half
+__host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
 
 template <int D, bool Q4>
 struct Cfg {
   static constexpr int kTileBytes = kBN * D * 2;          // one f16/bf16 K or V tile
-  static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kStages = Q4 ? 3 : (D == 128 ? 4 : 7);
-  static constexpr int kRawStages = Q4 ? 4 : 0;
+  static constexpr int kQBytes = kBM * D * 2;             // one Q tile
+  static constexpr int kStages = Q4 ? 3 : (D == 128 ? 4 : 6);
+  static constexpr int kRawStages = Q4 ? 3 : 0;
   static constexpr int kNibRow = D / 2;                   // bytes of nibbles per key
   static constexpr int kScaleRow = D / 32 * 2;            // bytes of scales per key
   static constexpr int kRawNib = kBN * kNibRow;
   static constexpr int kRawBytes = ((kRawNib + kBN * kScaleRow) + 1023) / 1024 * 1024;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffRing = kOffQ + kQBytes;
+  static constexpr int kOffQ = 0;                         // Q_A, Q_B
+  static constexpr int kOffRing = kOffQ + 2 * kQBytes;
   static constexpr int kOffRaw = kOffRing + kStages * kTileBytes;
   static constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
-  static constexpr int kWarps = Q4 ? 10 : 6;
+  static constexpr int kWarps = Q4 ? 16 : 12;
   static constexpr int kThreads = kWarps * 32;
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;     // O of tile A / B
 };
 
 // barrier slots (8 bytes each) inside the barrier area
 enum {
   kBarQFull = 0,
-  kBarSFull0 = 1,
-  kBarSFull1 = 2,
-  kBarPReady0 = 3,
-  kBarPReady1 = 4,
-  kBarODone0 = 5,     // PV(j) commits alternate between two barriers so that a waiter is
-  kBarDrain = 6,      // never two phases behind (parity waits alias two phases apart)
-  kBarODone1 = 7,
-  kBarRingFull = 8,    // + stage   (up to 8 stages)
+  kBarSFull = 1,       // + tile (2)
+  kBarPReady = 3,      // + tile (2)
+  kBarODone = 5,       // + tile (2): completes once, after the tile's last PV MMA
+  kBarDrain = 7,
+  kBarRingFull = 8,    // + stage (up to 8)
   kBarRingEmpty = 16,  // + stage
   kBarRawFull = 24,    // + raw stage
   kBarRawEmpty = 32,   // + raw stage
@@ -84,7 +89,7 @@ struct PrefillArgs {
   const uint8_t* k_scale;  // q4_0 only: fp16 scale planes [B, Hkv, Sk, D/32]
   const uint8_t* v_scale;
   int32_t* rescale_count;  // optional [B, Hq, Sq]
-  int B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, n_qtiles;
+  int B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, n_qtiles, n_pairs;
   float scale_log2;
 };
 
@@ -117,7 +122,7 @@ template <>
 struct Dq<true> {
   static __device__ __forceinline__ __nv_bfloat162 lo(uint32_t w, uint32_t mg) {
     uint32_t x = and_or<0x000F000Fu>(w, mg);  // 128 + n (mg = 0x43004300)
-    const uint32_t c = 0x43084308u;                 // 136
+    const uint32_t c = 0x43084308u;           // 136
     return __hsub2(*reinterpret_cast<__nv_bfloat162*>(&x),
                    *reinterpret_cast<const __nv_bfloat162*>(&c));
   }
@@ -134,6 +139,72 @@ struct Dq<true> {
     return *reinterpret_cast<uint32_t*>(&r);
   }
 };
+
+// Softmax over one 128-key block of one row (this thread's TMEM lane, columns scol..scol+127).
+// MASK: hide the keys with index > rel_lim (relative to the block); only blocks straddling the
+// diagonal or the key tail need it, the others use the branch-free instantiation.
+template <bool MASK>
+__device__ __forceinline__ float block_row_max(uint32_t scol, int rel_lim) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(scol + 64 * hf, r0);
+    tmem_ld32(scol + 64 * hf + 32, r1);
+    tmem_wait_ld();
+    reg_fence32(r0);
+    reg_fence32(r1);
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float a = __uint_as_float(r0[i]), c = __uint_as_float(r1[i]);
+      if (MASK) {
+        if (64 * hf + i > rel_lim) a = -INFINITY;
+        if (64 * hf + 32 + i > rel_lim) c = -INFINITY;
+      }
+      m0 = fmaxf(m0, a);
+      m1 = fmaxf(m1, c);
+    }
+    mx = fmaxf(mx, fmaxf(m0, m1));
+  }
+  return mx;
+}
+// P = 2^(s * sl2 + nf) for the block, packed in pairs over the first half of the S columns
+// (keys 32 c .. 32 c + 31 -> packed columns 16 c .. 16 c + 15, whose S values are already read);
+// returns the row sum of P.
+template <bool MASK, bool BF16>
+__device__ __forceinline__ float block_row_exp(uint32_t scol, int rel_lim, float sl2, float nf) {
+  float la = 0.f, lb = 0.f;
+#pragma unroll
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(scol + 32 * c, r);
+    tmem_wait_ld();
+    reg_fence32(r);
+    uint32_t pr[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+      if (MASK) {
+        if (32 * c + 2 * i > rel_lim) s0 = -INFINITY;
+        if (32 * c + 2 * i + 1 > rel_lim) s1 = -INFINITY;
+      }
+      const float p0 = ex2(fmaf(s0, sl2, nf)), p1 = ex2(fmaf(s1, sl2, nf));
+      if (i & 1) lb += p0 + p1; else la += p0 + p1;
+      pr[i] = pack2<BF16>(p0, p1);
+    }
+    tmem_st16(scol + 16 * c, pr);
+  }
+  return la + lb;
+}
+
+// number of 128-key blocks a query tile starting at row q0 must visit
+__device__ __forceinline__ int tile_blocks(const PrefillArgs& a, int q0) {
+  if (q0 >= a.Sq) return 0;
+  const int last_row = min(q0 + kBM - 1, a.Sq - 1);
+  const int kend = a.causal ? min(a.Sk, a.q_pos_offset + last_row + 1) : a.Sk;
+  return (kend + kBN - 1) / kBN;
+}
 
 template <int D, bool BF16, bool Q4>
 __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
@@ -152,24 +223,26 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // work unit: longest q tiles first (the slowest grid dimension enumerates q tiles)
+  // work unit: a pair of consecutive query tiles of one head, longest pairs first (the slowest
+  // grid dimension enumerates pairs); tile B may lie past Sq (odd tile count)
   const int h = blockIdx.x;
   const int b = blockIdx.y;
-  const int qtile = args.n_qtiles - 1 - static_cast<int>(blockIdx.z);
-  const int q0 = qtile * kBM;
+  const int pair = args.n_pairs - 1 - static_cast<int>(blockIdx.z);
+  const int q0A = 2 * pair * kBM;
+  const int q0B = q0A + kBM;
   const int g = h / (args.Hq / args.Hkv);
-  const int last_row = min(q0 + kBM - 1, args.Sq - 1);
-  const int kend = args.causal ? min(args.Sk, args.q_pos_offset + last_row + 1) : args.Sk;
-  const int nb = (kend + kBN - 1) / kBN;
+  const int nbA = tile_blocks(args, q0A);
+  const int nbB = tile_blocks(args, q0B);
+  const int nbmax = max(nbA, nbB);  // causal rows further down see at least as many keys
+  const bool hasB = q0B < args.Sq;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarSFull0), 1);
-    mbar_init(bar(kBarSFull1), 1);
-    mbar_init(bar(kBarPReady0), 128);
-    mbar_init(bar(kBarPReady1), 128);
-    mbar_init(bar(kBarODone0), 1);
-    mbar_init(bar(kBarODone1), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kBarSFull + t), 1);
+      mbar_init(bar(kBarPReady + t), 128);
+      mbar_init(bar(kBarODone + t), 1);
+    }
     mbar_init(bar(kBarDrain), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(kBarRingFull + s), Q4 ? 128 : 1);
@@ -200,12 +273,13 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
     }
     bool ok = true;
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(kBarQFull), C::kQBytes);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sbase + C::kOffQ + c * (kBM * 128), &tm_q, bar(kBarQFull), c * 64, q0,
-                    b * args.Hq + h);
+      mbar_arrive_expect_tx(bar(kBarQFull), (hasB ? 2 : 1) * C::kQBytes);
+      for (int t = 0; t < (hasB ? 2 : 1); ++t)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (kBM * 128), &tm_q,
+                      bar(kBarQFull), c * 64, t ? q0B : q0A, b * args.Hq + h);
     }
-    // tiles in the order the MMA consumes them: K0, K1, V0, K2, V1, K3, ...
+    // tiles in the order the MMA first uses them: K0, V0, K1, V1, ...
     int n = 0;
     auto produce = [&](bool is_v, int j) {
       if (!ok) return;
@@ -257,11 +331,9 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
       }
       ++n;
     };
-    produce(false, 0);
-    if (nb > 1) produce(false, 1);
-    for (int j = 0; j < nb; ++j) {
+    for (int j = 0; j < nbmax; ++j) {
+      produce(false, j);
       produce(true, j);
-      if (j + 2 < nb) produce(false, j + 2);
     }
     if (!ok && lane == 0) {
       // let copies already issued land before the CTA's shared memory goes away
@@ -280,56 +352,69 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
       constexpr uint32_t idesc_pv = make_idesc_f16(kBM, D, BF16, true);
       bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, &g_prefill_error);
       tc_fence_after();
-      const uint32_t qaddr = sbase + C::kOffQ;
       int n = 0;
       auto acquire = [&]() -> int {
         const int s = n % C::kStages;
         if (ok) ok = mbar_wait(bar(kBarRingFull + s), (n / C::kStages) & 1, abort_flag,
                                &g_prefill_error);
         tc_fence_after();
+        ++n;
         return s;
       };
-      auto release = [&](int s) {
-        mma_commit(bar(kBarRingEmpty + s));
-        ++n;
-      };
-      auto issue_qk = [&](int j) {
-        const int s = acquire();
-        if (!ok) return;
+      auto release = [&](int s) { mma_commit(bar(kBarRingEmpty + s)); };
+      auto issue_qk = [&](int t, int s) {
+        const uint32_t qaddr = sbase + C::kOffQ + t * C::kQBytes;
         const uint32_t kaddr = sbase + C::kOffRing + s * C::kTileBytes;
-        const uint32_t dcol = tmem + ((j & 1) ? kColS1 : kColS0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          const uint64_t ad = make_sdesc_sw128(qaddr + off, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(kaddr + off, 16, 1024);
-          mma_ss(dcol, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + col_s(t), make_sdesc_sw128(qaddr + off, 16, 1024),
+                 make_sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        release(s);
-        mma_commit(bar((j & 1) ? kBarSFull1 : kBarSFull0));
+        mma_commit(bar(kBarSFull + t));
       };
-      auto issue_pv = [&](int j) {
-        const int s = acquire();
-        if (!ok) return;
-        ok = mbar_wait(bar((j & 1) ? kBarPReady1 : kBarPReady0), (j >> 1) & 1, abort_flag,
-                       &g_prefill_error);
+      auto issue_pv = [&](int t, int j, int s, int nb_t) {
+        ok = ok && mbar_wait(bar(kBarPReady + t), j & 1, abort_flag, &g_prefill_error);
         if (!ok) return;
         tc_fence_after();
         const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
-        const uint32_t pcol = tmem + ((j & 1) ? kColS1 : kColS0);
+        const uint32_t ocol = t ? C::kColO1 : C::kColO0;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bd = make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024);
-          mma_ts(tmem + kColO, pcol + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        release(s);
-        mma_commit(bar((j & 1) ? kBarODone1 : kBarODone0));
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + ocol, tmem + col_s(t) + kk * 8,
+                 make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        if (j == nb_t - 1) mma_commit(bar(kBarODone + t));
       };
-      if (ok) issue_qk(0);
-      if (ok && nb > 1) issue_qk(1);
-      for (int j = 0; j < nb && ok; ++j) {
-        issue_pv(j);
-        if (ok && j + 2 < nb) issue_qk(j + 2);
+      // order: QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage is
+      // acquired at its first use and released after its last (all in ring order).
+      if (nbmax > 0 && ok) {
+        const int sK = acquire();
+        if (ok) {
+          if (nbA > 0) issue_qk(0, sK);
+          if (nbB > 0) issue_qk(1, sK);
+          release(sK);
+        }
+      }
+      for (int j = 0; j < nbmax && ok; ++j) {
+        const int sV = acquire();
+        if (!ok) break;
+        if (j < nbA) issue_pv(0, j, sV, nbA);
+        if (!ok) break;
+        const bool next = j + 1 < nbmax;
+        int sK = 0;
+        if (next) {
+          sK = acquire();
+          if (!ok) break;
+          if (j + 1 < nbA) issue_qk(0, sK);
+        }
+        if (j < nbB) issue_pv(1, j, sV, nbB);
+        if (!ok) break;
+        release(sV);
+        if (next) {
+          if (j + 1 < nbB) issue_qk(1, sK);
+          release(sK);
+        }
       }
       if (!ok) {
         // wait until every MMA issued so far has finished before TMEM is released
@@ -338,48 +423,37 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
         mbar_wait(bar(kBarDrain), 0, &never, nullptr, kWaitLimitNs);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------------- softmax rows
+    const int t = (warp >= 8) ? 1 : 0;  // query tile
+    const int nb = t ? nbB : nbA;
+    const int q0 = t ? q0B : q0A;
     const int row = 32 * (warp & 3) + lane;
     const int qrow = q0 + row;
     const int pos = args.q_pos_offset + qrow;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t scol = tmem + lane_off + col_s(t);
+    const uint32_t ocol = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
     const float sl2 = args.scale_log2;
     float f = -INFINITY;  // frame, base-2 units of the scaled score
     float l = 0.f;
     int nres = 0;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
-      const uint32_t scol = (j & 1) ? kColS1 : kColS0;
-      ok = mbar_wait(bar((j & 1) ? kBarSFull1 : kBarSFull0), (j >> 1) & 1, abort_flag,
-                     &g_prefill_error);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      float s[kBN];
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          tmem_ld32(tmem + lane_off + scol + 32 * c, r);
-          tmem_wait_ld();
-          reg_fence32(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
-        }
+      ok = mbar_wait(bar(kBarSFull + t), j & 1, abort_flag, &g_prefill_error);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
       }
+      tc_fence_after();
       const int kb = j * kBN;
       const bool need_mask =
           (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
-      if (need_mask) {
-        const int lim = args.causal ? min(args.Sk - 1, pos) : args.Sk - 1;
-#pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (kb + i > lim) s[i] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      // last visible key of this row, relative to the block
+      const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
+      // pass 1: row max over the 128 scores
+      const float mx = need_mask ? block_row_max<true>(scol, rel_lim)
+                                 : block_row_max<false>(scol, rel_lim);
       const float m2 = mx * sl2;
       const bool need = m2 > f + kMarginLog2;
       if (__any_sync(0xffffffffu, need)) {
@@ -389,50 +463,36 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
           f = m2;
           ++nres;
         }
+        // S(j) being ready means PV(j-1) has completed (QK(j) was issued after it), so O can be
+        // rescaled in place without a further wait
         if (j > 0) {
-          // O holds the blocks before j; PV(j-1) must have landed before it is rescaled
-          ok = mbar_wait(bar(((j - 1) & 1) ? kBarODone1 : kBarODone0), ((j - 1) >> 1) & 1,
-                         abort_flag, &g_prefill_error);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_off + kColO + 32 * c, r);
+            tmem_ld32(ocol + 32 * c, r);
             tmem_wait_ld();
+            reg_fence32(r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tmem + lane_off + kColO + 32 * c, r);
+            tmem_st32(ocol + 32 * c, r);
           }
           tmem_wait_st();
         }
       }
-      // P = 2^(t - f) packed in pairs over S
+      // pass 2: P = 2^(t - f) over the first half of S, row sum
       const float nf = -f;
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t pr[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[32 * c + 2 * i], sl2, nf));
-          const float p1 = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, nf));
-          l += p0 + p1;
-          pr[i] = pack2<BF16>(p0, p1);
-        }
-        tmem_st16(tmem + lane_off + scol + 16 * c, pr);
-      }
+      l += need_mask ? block_row_exp<true, BF16>(scol, rel_lim, sl2, nf)
+                     : block_row_exp<false, BF16>(scol, rel_lim, sl2, nf);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar((j & 1) ? kBarPReady1 : kBarPReady0));
+      mbar_arrive(bar(kBarPReady + t));
     }
-    if (ok) {
-      // PV(nb-1) done implies every earlier MMA is done (one commit tracks all of them)
-      ok = mbar_wait(bar(((nb - 1) & 1) ? kBarODone1 : kBarODone0), ((nb - 1) >> 1) & 1,
-                     abort_flag, &g_prefill_error);
+    if (ok && nb > 0) {
+      // the tile's last PV MMA completing implies all of its MMAs have
+      ok = mbar_wait(bar(kBarODone + t), 0, abort_flag, &g_prefill_error);
       ok = __all_sync(0xffffffffu, ok);
     }
-    if (ok) {
+    if (ok && nb > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool store = qrow < args.Sq;
@@ -441,8 +501,9 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kColO + 32 * c, r);
+        tmem_ld32(ocol + 32 * c, r);
         tmem_wait_ld();
+        reg_fence32(r);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -459,65 +520,68 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
         args.rescale_count[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = nres;
     }
   } else if constexpr (Q4) {
-    // ---------------------------------------------------------------- q4_0 dequant
-    // thread t expands key row t of each raw tile into the 128B-swizzled f16/bf16 ring stage
-    const int t = threadIdx.x - 6 * 32;
-    const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
-    bool ok = true;
-    const int ntiles = 2 * nb;
-    for (int n = 0; n < ntiles; ++n) {
-      const int rs = n % C::kRawStages;
-      const int s = n % C::kStages;
-      ok = mbar_wait(bar(kBarRawFull + rs), (n / C::kRawStages) & 1, abort_flag,
-                     &g_prefill_error);
-      if (ok && n >= C::kStages)
-        ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+    if (warp >= 12) {
+      // -------------------------------------------------------------- q4_0 dequant
+      // thread t expands key row t of each raw tile into the 128B-swizzled f16/bf16 ring stage
+      const int t = threadIdx.x - 12 * 32;
+      const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
+      bool ok = true;
+      const int ntiles = 2 * nbmax;
+      for (int n = 0; n < ntiles; ++n) {
+        const int rs = n % C::kRawStages;
+        const int s = n % C::kStages;
+        ok = mbar_wait(bar(kBarRawFull + rs), (n / C::kRawStages) & 1, abort_flag,
                        &g_prefill_error);
-      if (!ok) break;
-      const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
-      const uint8_t* nrow = raw + t * C::kNibRow;
-      const __half* srow = reinterpret_cast<const __half*>(raw + C::kRawNib + t * C::kScaleRow);
-      uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
+        if (ok && n >= C::kStages)
+          ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                         &g_prefill_error);
+        if (!ok) break;
+        const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
+        const uint8_t* nrow = raw + t * C::kNibRow;
+        const __half* srow =
+            reinterpret_cast<const __half*>(raw + C::kRawNib + t * C::kScaleRow);
+        uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
 #pragma unroll
-      for (int blk = 0; blk < D / 32; ++blk) {
-        // 16 bytes of nibbles of this key, 64B-swizzled (D=128) or 32B-swizzled (D=64) by TMA
-        const int chunk = (D == 128) ? (blk ^ ((t >> 1) & 3)) : (blk ^ ((t >> 2) & 1));
-        const uint4 wv = *reinterpret_cast<const uint4*>(nrow + 16 * chunk);
-        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-        const __half dh = srow[blk];
-        uint32_t outv[16];  // 32 dequantized elements, packed in pairs, natural order
+        for (int blk = 0; blk < D / 32; ++blk) {
+          // 16 bytes of nibbles of this key, 64B-swizzled (D=128) or 32B-swizzled (D=64)
+          const int chunk = (D == 128) ? (blk ^ ((t >> 1) & 3)) : (blk ^ ((t >> 2) & 1));
+          const uint4 wv = *reinterpret_cast<const uint4*>(nrow + 16 * chunk);
+          const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+          const __half dh = srow[blk];
+          uint32_t outv[16];  // 32 dequantized elements, packed in pairs, natural order
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          // bytes 4q..4q+3 -> elements 4q..4q+3 (low) and 4q+16..4q+19 (high)
-          const uint32_t a = __byte_perm(w[q], 0u, 0x5150);  // byte0 at b0, byte1 at b2
-          const uint32_t c2 = __byte_perm(w[q], 0u, 0x5352); // byte2 at b0, byte3 at b2
-          if (BF16) {
-            const float d = __half2float(dh);
-            outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a, mg), d);
-            outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2, mg), d);
-            outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a, mg), d);
-            outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2, mg), d);
-          } else {
-            outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a, mg), dh);
-            outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2, mg), dh);
-            outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a, mg), dh);
-            outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2, mg), dh);
+          for (int q = 0; q < 4; ++q) {
+            // bytes 4q..4q+3 -> elements 4q..4q+3 (low) and 4q+16..4q+19 (high)
+            const uint32_t a = __byte_perm(w[q], 0u, 0x5150);   // byte0 at b0, byte1 at b2
+            const uint32_t c2 = __byte_perm(w[q], 0u, 0x5352);  // byte2 at b0, byte3 at b2
+            if (BF16) {
+              const float d = __half2float(dh);
+              outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a, mg), d);
+              outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2, mg), d);
+              outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a, mg), d);
+              outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2, mg), d);
+            } else {
+              outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a, mg), dh);
+              outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2, mg), dh);
+              outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a, mg), dh);
+              outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2, mg), dh);
+            }
+          }
+          // elements 32 blk + 8 cc .. +7 form 16-byte chunk (4 blk + cc) of the row
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int col16 = 4 * blk + cc;        // 16-byte chunk index along D
+            const int atom = col16 >> 3;           // 64-element swizzle atom
+            const int ch = (col16 & 7) ^ (t & 7);  // 128B swizzle
+            *reinterpret_cast<uint4*>(dst + atom * (kBN * 128) + t * 128 + ch * 16) =
+                make_uint4(outv[4 * cc], outv[4 * cc + 1], outv[4 * cc + 2], outv[4 * cc + 3]);
           }
         }
-        // elements 32 blk + 8 cc .. +7 form 16-byte chunk (4 blk + cc) of the row
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int col16 = 4 * blk + cc;       // 16-byte chunk index along D
-          const int atom = col16 >> 3;          // 64-element swizzle atom
-          const int ch = (col16 & 7) ^ (t & 7); // 128B swizzle
-          *reinterpret_cast<uint4*>(dst + atom * (kBN * 128) + t * 128 + ch * 16) =
-              make_uint4(outv[4 * cc], outv[4 * cc + 1], outv[4 * cc + 2], outv[4 * cc + 3]);
-        }
+        // generic-proxy writes must be visible to the tensor core's async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(bar(kBarRingFull + s));
+        mbar_arrive(bar(kBarRawEmpty + rs));
       }
-      // generic-proxy writes must be visible to the tensor core's async proxy
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(bar(kBarRingFull + s));
-      mbar_arrive(bar(kBarRawEmpty + rs));
     }
   }
 
@@ -555,8 +619,9 @@ static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   a.q_pos_offset = L.q_pos_offset;
   a.causal = L.causal;
   a.n_qtiles = (L.Sq + kBM - 1) / kBM;
+  a.n_pairs = (a.n_qtiles + 1) / 2;
   a.scale_log2 = L.scale * kLog2e;
-  dim3 grid(L.Hq, L.B, a.n_qtiles);
+  dim3 grid(L.Hq, L.B, a.n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, a);
   return cudaGetLastError();
 }
