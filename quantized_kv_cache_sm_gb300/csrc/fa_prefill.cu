@@ -23,13 +23,12 @@
 //    exceeds f by more than 10 natural-log units; only then are O and l multiplied by
 //    e^(f_old - f_new).  P stays below e^10 = 22026 in every frame.
 //
-// Warp roles (dense: 12 warps; q4_0: 16 warps):
+// Warp roles (12 warps):
 //   warp 0       TMA producer (one lane)
 //   warp 1       TMEM allocator + MMA issuer (one lane)
-//   warps 2, 3   idle
+//   warps 2, 3   q4_0 dequant (q4_0 variant only; idle otherwise), two key rows per thread
 //   warps 4..7   softmax / rescale / epilogue of query tile A, one row per thread
 //   warps 8..11  the same for query tile B
-//   warps 12..15 q4_0 dequant (q4_0 variant only), one key row per thread
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -63,7 +62,7 @@ struct Cfg {
   static constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
-  static constexpr int kWarps = Q4 ? 16 : 12;
+  static constexpr int kWarps = 12;
   static constexpr int kThreads = kWarps * 32;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;     // O of tile A / B
 };
@@ -245,12 +244,12 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
     }
     mbar_init(bar(kBarDrain), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(kBarRingFull + s), Q4 ? 128 : 1);
+      mbar_init(bar(kBarRingFull + s), Q4 ? 64 : 1);  // dequant threads, or the TMA lane
       mbar_init(bar(kBarRingEmpty + s), 1);
     }
     for (int s = 0; s < C::kRawStages; ++s) {
       mbar_init(bar(kBarRawFull + s), 1 + 32);  // TMA lane + 32 cp.async arrivals
-      mbar_init(bar(kBarRawEmpty + s), 128);
+      mbar_init(bar(kBarRawEmpty + s), 64);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -520,10 +519,11 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
         args.rescale_count[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = nres;
     }
   } else if constexpr (Q4) {
-    if (warp >= 12) {
+    if (warp == 2 || warp == 3) {
       // -------------------------------------------------------------- q4_0 dequant
-      // thread t expands key row t of each raw tile into the 128B-swizzled f16/bf16 ring stage
-      const int t = threadIdx.x - 12 * 32;
+      // thread u expands key rows u and u + 64 of each raw tile into the 128B-swizzled
+      // f16/bf16 ring stage
+      const int u = threadIdx.x - 2 * 32;
       const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
       bool ok = true;
       const int ntiles = 2 * nbmax;
@@ -537,10 +537,13 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
                          &g_prefill_error);
         if (!ok) break;
         const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
+        uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
+#pragma unroll 1
+        for (int rr = 0; rr < 2; ++rr) {
+        const int t = u + 64 * rr;  // key row within the tile
         const uint8_t* nrow = raw + t * C::kNibRow;
         const __half* srow =
             reinterpret_cast<const __half*>(raw + C::kRawNib + t * C::kScaleRow);
-        uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
 #pragma unroll
         for (int blk = 0; blk < D / 32; ++blk) {
           // 16 bytes of nibbles of this key, 64B-swizzled (D=128) or 32B-swizzled (D=64)
@@ -576,6 +579,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
             *reinterpret_cast<uint4*>(dst + atom * (kBN * 128) + t * 128 + ch * 16) =
                 make_uint4(outv[4 * cc], outv[4 * cc + 1], outv[4 * cc + 2], outv[4 * cc + 3]);
           }
+        }
         }
         // generic-proxy writes must be visible to the tensor core's async proxy
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
