@@ -349,8 +349,8 @@ def decode_leg(fa, dev, stream, peaks, peaks_src):
     return {
         "workload": w.name, "metric": "q4_0 decode KV GB/s", "value": round(gbs, 1),
         "unit": "GB/s", "ms_per_call": round(ms, 5), "kv_bytes_per_call": nbytes,
-        "launches_per_call": 2,
-        "roofline": {"kernel": "decode_split_kernel + decode_combine_kernel (one call)",
+        "launches_per_call": 1,
+        "roofline": {"kernel": "decode_split_kernel (one call: splits and their merge)",
                      "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                      "peak_source": f"{peaks_src} HBM copy",

@@ -79,7 +79,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, in
 /* fa_fwd with caller-provided scratch and an optional rescale counter.
  *  workspace, workspace_bytes : device buffer of at least fa_workspace_bytes(...) bytes (may be
  *                 NULL when that is 0); owned by the caller, must not be used by another call in
- *                 flight at the same time.
+ *                 flight at the same time.  Its contents on entry do not matter: it holds one
+ *                 32-bit arrival flag per split of each (batch, kv head), which the split sets
+ *                 to a tag drawn afresh for every call once its partial result is stored, then
+ *                 the partial results, which the split that finds all its siblings' flags set
+ *                 merges (it also clears those flags).  A call reads only what it wrote itself,
+ *                 apart from the flags; a stale flag is mistaken for this call's only if it
+ *                 holds exactly the call's 32-bit tag.
  *  rescale_count : optional device int32 [B, Hq, Sq] (NULL to skip).  The prefill kernel writes
  *                 for every query row how many times its softmax frame was moved (the first
  *                 key block always sets it, so every value is >= 1); the deferred rescale of
@@ -106,13 +112,15 @@ size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_p
  * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *  Arguments: as fa_fwd with Sq = 1 (q, o: [B, Hq, 1, D]; k, v: [B, Hkv, Sk, D] dense or q4_0).
  *  Limit: shapes whose fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal) exceeds
- *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED (for D = 128 that is
- *    B * Hq * nsplit > 7943, nsplit being the split count the decode plan picks: about
- *    3 * SM count / (B * Hkv), at least 1); invalid shapes give FA_ERR_INVALID_ARG.
+ *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED.  That size is
+ *    4 * B * Hkv * nsplit rounded up to a multiple of 256, plus 4 * (D + 4) * B * Hq * nsplit,
+ *    nsplit being the split count the decode plan picks (about 3 * SM count / (B * Hkv), at
+ *    least 1): for D = 128 roughly B * Hq * nsplit <= 7900.  Invalid shapes give
+ *    FA_ERR_INVALID_ARG.
  *  First call per device: it looks up the array's device address (cudaGetSymbolAddress) with
  *    that device current, so make the first call on each device before any stream capture.
  *  Sharing: every call on a device uses the same array and leaves its contents behind.  Nothing
- *    in it needs clearing (each call writes every entry it later reads), but calls whose
+ *    in it needs clearing (see the workspace of fa_fwd_ex), but calls whose
  *    execution overlaps on the GPU -- on different streams, or from different host threads --
  *    race on the array and produce wrong results; order them on one stream or with events. */
 fa_status fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, int B,

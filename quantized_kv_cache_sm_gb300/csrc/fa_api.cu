@@ -1,5 +1,6 @@
 // C-ABI front end: argument checks, TMA descriptors, kernel dispatch, device status.
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -103,7 +104,22 @@ size_t workspace_for(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_of
   decode_plan(B, Hkv, sk_eff, num_sms(), q4, &ns, &ck);
   if (nsplit_out) *nsplit_out = ns;
   if (chunk_out) *chunk_out = ck;
-  return static_cast<size_t>(B) * Hq * ns * (D + 4) * sizeof(float);
+  return decode_flag_bytes(B, Hkv, ns) +
+         static_cast<size_t>(B) * Hq * ns * (D + 4) * sizeof(float);
+}
+
+// a call tag for the decode arrival flags: nonzero and unlike any nearby call's, and unlike
+// small integers or common float bit patterns that a reused buffer may still hold
+uint32_t next_call_tag() {
+  static std::atomic<uint64_t> calls{0};
+  uint64_t z = calls.fetch_add(1, std::memory_order_relaxed) + 0x9e3779b97f4a7c15ull;
+  // 64-bit finalizer of SplitMix64 (Steele, Lea, Flood, "Fast splittable pseudorandom number
+  // generators", OOPSLA 2014)
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  z ^= z >> 31;
+  const uint32_t t = static_cast<uint32_t>(z >> 32);
+  return t ? t : 1u;
 }
 
 // enough decode scratch for either cache format
@@ -196,7 +212,10 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
     if (!ok) return FA_ERR_CUDA;
     L.q = q;
     L.o = o;
-    L.partial = static_cast<float*>(workspace);
+    L.flags = static_cast<uint32_t*>(workspace);
+    L.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                         decode_flag_bytes(B, Hkv, nsplit));
+    L.tag = next_call_tag();
     L.B = B;
     L.Hq = Hq;
     L.Hkv = Hkv;

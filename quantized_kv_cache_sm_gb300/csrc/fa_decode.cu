@@ -21,7 +21,10 @@
 //  * each consumer warp keeps its own online softmax state over 16 or 32 keys per step; the warps
 //    of a CTA merge through shared memory and write one partial (m, l, unnormalised O) per query
 //    head and split;
-//  * a combine kernel merges the splits: M = max m_s, O = sum e^(m_s - M) O_s / sum e^(m_s - M) l_s.
+//  * the splits of one (batch, kv head) merge inside the same launch: each CTA publishes its
+//    partials and an arrival flag, reads the flags of its sibling splits, and a CTA that finds
+//    them all set computes M = max m_s, O = sum e^(m_s - M) O_s / sum e^(m_s - M) l_s from L2.
+//    No second kernel, and no gap between two launches, sits on the decode step.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -55,7 +58,8 @@ struct DCfg {
   static constexpr int kStages = Q4 ? (D == 128 ? 3 : 6) : (D == 128 ? 3 : 6);
   static constexpr int kCtasPerSm = Q4 ? 3 : 2;
   static constexpr int kOffBar = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr int kOffQ = kOffBar + 256;  // the group's query rows, [8][D] 16-bit
+  static constexpr int kSmemBytes = kOffQ + 8 * D * 2 + 1024;
   static constexpr int kThreads = 32 * (1 + kConsumers);
   static constexpr int kPartStride = D + 4;  // m, l, pad, pad, O[D]
   // cross-warp merge buffer (reuses the stages): per warp 8 heads x (D + 2) floats
@@ -172,9 +176,16 @@ __device__ __forceinline__ uint16_t f2h(float v) {
 
 struct DecodeArgs {
   const uint16_t* q;
+  uint16_t* o;
   const uint8_t* k_scale;
   const uint8_t* v_scale;
   float* partial;
+  // arrival flags [B, Hkv, nsplit]: a split that has published its partials stores this call's
+  // tag in its flag.  A flag holding anything else counts as not arrived, so the workspace needs
+  // no clearing; a merging CTA sets its flags back to 0, so a replay of the same launch (same
+  // tag) starts from cleared flags too.
+  uint32_t* flags;
+  uint32_t tag;
   int Hq, Hkv, Sk, Sk_eff, nsplit, chunk;
   float scale_log2;
 };
@@ -214,7 +225,6 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -349,8 +359,14 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
   // values' constant offsets (f16: 1032 on low halves, 72 on high halves; bf16: 136)
   float corr[kNB][2];
   {
-    const int hq = hkv * G + g8;
-    const uint16_t* qrow = args.q + (static_cast<int64_t>(b) * args.Hq + hq) * D;
+    // the G query rows of this group are contiguous: stage them in shared memory with one
+    // 16-byte load per thread, then build the fragments from there
+    const uint16_t* qsrc = args.q + (static_cast<int64_t>(b) * args.Hq + hkv * G) * D;
+    uint16_t* qs = reinterpret_cast<uint16_t*>(sgen + C::kOffQ);
+    for (int idx = threadIdx.x - 32; idx < G * D / 8; idx += 32 * kConsumers)
+      reinterpret_cast<uint4*>(qs)[idx] = __ldg(reinterpret_cast<const uint4*>(qsrc) + idx);
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
+    const uint16_t* qrow = qs + g8 * D;
     const bool valid = g8 < G;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
@@ -381,10 +397,10 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
       for (int blk = 0; blk < kNB; ++blk) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int h2 = hkv * G + 2 * t4 + hh;
           float lo = 0.f, hi = 0.f;
           if (2 * t4 + hh < G) {
-            const uint16_t* qr = args.q + (static_cast<int64_t>(b) * args.Hq + h2) * D + 32 * blk;
+            const uint16_t* qr = qs + (2 * t4 + hh) * D + 32 * blk;
+#pragma unroll
             for (int i = 0; i < 16; ++i) {
               lo += h2f<BF16>(qr[i]);
               hi += h2f<BF16>(qr[16 + i]);
@@ -659,6 +675,7 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
   }
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
   const int tid = threadIdx.x - 32;  // 0..127
+  const int64_t row0 = static_cast<int64_t>(b) * args.Hq + static_cast<int64_t>(hkv) * G;
   for (int idx = tid; idx < G * (D + 2); idx += 32 * kConsumers) {
     const int hh = idx / (D + 2);
     const int c = idx % (D + 2);
@@ -678,63 +695,111 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
       }
       out = acc;
     }
-    const int hq = hkv * G + hh;
-    float* dst = args.partial +
-                 ((static_cast<int64_t>(b) * args.Hq + hq) * args.nsplit + split) * C::kPartStride;
+    float* dst = args.partial + ((row0 + hh) * args.nsplit + split) * C::kPartStride;
     dst[c == 0 ? 0 : (c == 1 ? 1 : c + 2)] = out;
   }
-}
 
-constexpr int kMaxCombineSplits = 1024;
-
-template <int D, bool BF16>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const float* partial,
-                                                             uint16_t* __restrict__ o, int nsplit) {
-  constexpr int kStride = D + 4;
-  __shared__ float wsm[kMaxCombineSplits];  // e^(m_s - M) per split
-  __shared__ float red[2][4];
-  const int64_t row = blockIdx.x;  // b * Hq + hq
-  const float* p = partial + row * nsplit * kStride;
-  pdl_wait_primary();  // the split kernel's partials are complete and visible
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // M = max m_s
-  float M = -INFINITY;
-  for (int s = tid; s < nsplit; s += blockDim.x) M = fmaxf(M, p[s * kStride]);
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) red[0][warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-  // weights and L = sum e^(m_s - M) l_s
-  float L = 0.f;
-  for (int s = tid; s < nsplit; s += blockDim.x) {
-    const float ms = p[s * kStride];
-    const float wgt = (ms == -INFINITY) ? 0.f : ex2(ms - M);
-    wsm[s] = wgt;
-    L += wgt * p[s * kStride + 1];
+  // ------------------------------------------------------------------ merge the splits
+  // After a barrier over the consumer threads one thread publishes this split's flag with a
+  // gpu-scope release store (cumulative: it covers the partial stores of every thread that
+  // reached the barrier), orders that store before its loads with a sequentially consistent
+  // fence, and one warp loads the flags of every split of this (batch, kv head).  Of two splits
+  // that publish at the same time at least one sees the other's flag (the fence forbids both
+  // missing), so at least one CTA finds all flags set; every CTA that does merges, and they all
+  // write the same bytes.  No CTA waits for another and no atomic read-modify-write is contended.
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
+  volatile uint32_t* is_last =
+      reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 16 * C::kStages + 8);
+  uint32_t* flags = args.flags + bh * args.nsplit;
+  if (cw == 0) {
+    if (lane == 0) st_release_gpu(flags + split, args.tag);
+    __syncwarp();
+    fence_sc_gpu();  // the whole warp: its flag loads below come after the store above
+    bool all = true;
+    for (int s = lane; s < args.nsplit; s += 32) all = all && ld_relaxed_gpu(flags + s) == args.tag;
+    all = __all_sync(0xffffffffu, all);
+    if (all) fence_acq_rel_gpu();  // the partials behind the flags are read after this
+    if (lane == 0) *is_last = all ? 1u : 0u;
   }
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  if (lane == 0) red[1][warp] = L;
-  __syncthreads();
-  L = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  const float inv = 1.f / L;
-  for (int d = tid; d < D; d += blockDim.x) {
-    // eight independent loads in flight per thread
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int s = 0;
-    for (; s + 8 <= nsplit; s += 8) {
-      float v[8];
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
+  if (*is_last == 0u) return;
+  if (cw == 0)
+    for (int s = lane; s < args.nsplit; s += 32) st_relaxed_gpu(flags + s, 0u);
+  constexpr int kPer = D / 32;  // head-dim elements per lane
+  constexpr int kStride = C::kPartStride;
+  for (int hh = cw; hh < G; hh += kConsumers) {
+    const float* p = args.partial + (row0 + hh) * args.nsplit * kStride;
+    // (m_s, l_s) with the splits across the lanes, 32 at a time; the first 32 stay in registers
+    float2 ml0 = make_float2(-INFINITY, 0.f);
+    if (lane < args.nsplit) ml0 = __ldcg(reinterpret_cast<const float2*>(p + lane * kStride));
+    float M = ml0.x;
+    for (int s = lane + 32; s < args.nsplit; s += 32) M = fmaxf(M, __ldcg(p + s * kStride));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = p[(s + j) * kStride + 4 + d];
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    float acc[kPer];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = fmaf(wsm[s + j], v[j], acc[j]);
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    for (int s0 = 0; s0 < args.nsplit; s0 += 32) {
+      float2 ml = ml0;
+      if (s0 > 0) {
+        ml = make_float2(-INFINITY, 0.f);
+        if (s0 + lane < args.nsplit)
+          ml = __ldcg(reinterpret_cast<const float2*>(p + (s0 + lane) * kStride));
+      }
+      const float wl = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);  // e^(m_s - M), lane s
+      L = fmaf(wl, ml.y, L);
+      const int n = min(32, args.nsplit - s0);
+      // O_s rows, eight splits' loads in flight before their multiply-adds (in split order)
+      for (int j0 = 0; j0 < n; j0 += 8) {
+        float x[8][kPer];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float* row = p + (s0 + j0 + j) * kStride + 4;
+          if (j0 + j < n) {
+            if constexpr (kPer == 4) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(row) + lane);
+              x[j][0] = v.x; x[j][1] = v.y; x[j][2] = v.z; x[j][3] = v.w;
+            } else {
+              const float2 v = __ldcg(reinterpret_cast<const float2*>(row) + lane);
+              x[j][0] = v.x; x[j][1] = v.y;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) x[j][e] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) acc[e] = fmaf(wj, x[j][e], acc[e]);
+        }
+      }
     }
-    for (; s < nsplit; ++s) acc[0] = fmaf(wsm[s], p[s * kStride + 4 + d], acc[0]);
-    const float tot = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-    o[row * D + d] = f2h<BF16>(tot * inv);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float inv = 1.f / L;
+    uint16_t* dst = args.o + (row0 + hh) * D + lane * kPer;
+    const uint32_t w0 = static_cast<uint32_t>(f2h<BF16>(acc[0] * inv)) |
+                        (static_cast<uint32_t>(f2h<BF16>(acc[1] * inv)) << 16);
+    if constexpr (kPer == 4) {
+      const uint32_t w1 = static_cast<uint32_t>(f2h<BF16>(acc[2] * inv)) |
+                          (static_cast<uint32_t>(f2h<BF16>(acc[3] * inv)) << 16);
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = w0;
+    }
   }
 }
+
+constexpr int kMaxSplits = 1024;  // splits per (batch, kv head)
 
 }  // namespace
+
+size_t decode_flag_bytes(int B, int Hkv, int nsplit) {
+  return (static_cast<size_t>(B) * Hkv * nsplit * sizeof(uint32_t) + 255) / 256 * 256;
+}
 
 int decode_tile_keys(bool q4) {
   return q4 ? DCfg<128, true>::kTileKeys : DCfg<128, false>::kTileKeys;
@@ -749,7 +814,7 @@ void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool q4, int* nsplit, 
   if (ns < 1) ns = 1;
   const int max_tiles = (Sk_eff + tile - 1) / tile;
   if (ns > max_tiles) ns = max_tiles;
-  if (ns > kMaxCombineSplits) ns = kMaxCombineSplits;
+  if (ns > kMaxSplits) ns = kMaxSplits;
   if (ns < 1) ns = 1;
   int ck = (Sk_eff + ns - 1) / ns;
   ck = (ck + tile - 1) / tile * tile;
@@ -768,7 +833,10 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   a.q = static_cast<const uint16_t*>(L.q);
   a.k_scale = static_cast<const uint8_t*>(L.k_scale);
   a.v_scale = static_cast<const uint8_t*>(L.v_scale);
+  a.o = static_cast<uint16_t*>(L.o);
   a.partial = L.partial;
+  a.flags = L.flags;
+  a.tag = L.tag;
   a.Hq = L.Hq;
   a.Hkv = L.Hkv;
   a.Sk = L.Sk;
@@ -778,24 +846,6 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   a.scale_log2 = L.scale * kLog2e;
   dim3 grid(L.nsplit, L.Hkv, L.B);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // the combine kernel is a programmatic dependent of the split kernel: it is scheduled while
-  // the split kernel runs and waits (griddepcontrol.wait) for its partials
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(L.B * L.Hq);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, BF16>,
-                         static_cast<const float*>(L.partial), static_cast<uint16_t*>(L.o),
-                         L.nsplit);
-  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -26,13 +26,17 @@ struct DecodeLaunch {
   void* o;
   const void* k_scale;           // q4_0 only
   const void* v_scale;
+  uint32_t* flags;               // [B, Hkv, nsplit] arrival flags (workspace, offset 0)
   float* partial;                // [B, Hq, nsplit, D + 4] f32: m, l, pad, pad, O (workspace)
+  uint32_t tag;                  // nonzero, different for every call
   int B, Hq, Hkv, Sk_eff, Sk, D, nsplit, chunk;
   float scale;
   bool bf16, q4;
 };
 cudaError_t decode_launch(const DecodeLaunch& L, cudaStream_t stream);
 uint32_t decode_take_error();
+// decode scratch: the arrival flags, padded to 256 bytes, then the partials
+size_t decode_flag_bytes(int B, int Hkv, int nsplit);
 // decode work split for a given shape and cache format (shared by the workspace query and the
 // launch), and the keys per pipeline stage (the TMA box height)
 void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool q4, int* nsplit, int* chunk);

@@ -56,8 +56,8 @@ extern "C" fa_status fa_fwd_decode_noalloc(const void* q, const void* k, const v
   const size_t need = fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal);
   if (need == 0) return FA_ERR_INVALID_ARG;
   if (need > kNoallocScratchBytes) return FA_ERR_UNSUPPORTED;
-  // Every partial the combine kernel reads is written earlier in the same call, so the area
-  // needs no clearing between calls.
+  // Every partial the merging CTA reads is written earlier in the same call, and the arrival
+  // flags are tagged per call (and start as zeros here), so the area needs no clearing.
   return fa_fwd_ex(q, k, v, o, B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal, scale, dtype,
                    kv_format, scratch, kNoallocScratchBytes, nullptr, stream);
 }

@@ -74,3 +74,60 @@ def test_decode_ex_rejects_small_workspace(fa):
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd_ex(q, k, v, workspace=ws)
     assert e.value.status == fa.FA_ERR_INVALID_ARG
+
+
+def test_decode_workspace_contents_do_not_matter(fa):
+    """The splits of each (batch, kv head) are merged by a CTA that finds all its siblings'
+    arrival flags (kept in the workspace) set.  A workspace full of stale bytes (all ones,
+    random bytes, or left behind by a call of another shape and cache format) must give the
+    same result as a fresh one."""
+    shapes = [(2, 32, 8, 4097, 128, True, 4096, "f16", "q4_0"),
+              (1, 8, 2, 3001, 64, True, 3000, "bf16", "dense"),
+              (3, 12, 3, 999, 128, False, 0, "f16", "q4_0")]
+    need = max(fa.fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, off, c)
+               for (B, Hq, Hkv, Sk, D, c, off, _, _) in shapes)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    fills = [torch.full((need,), 255, dtype=torch.uint8, device="cuda"),
+             torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda", generator=g)]
+    for ws in fills:
+        for (B, Hq, Hkv, Sk, D, causal, off, dtype, kv) in shapes:
+            q, k, v = fa_inputs.make_tensors(B, Hq, Hkv, 1, Sk, D, dtype, seed=Sk, device="cuda")
+            if kv == "q4_0":
+                k, v = fa.fa_quantize_q4_0(k), fa.fa_quantize_q4_0(v)
+            fresh = torch.zeros(fa.fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, off, causal),
+                                dtype=torch.uint8, device="cuda")
+            want = fa.fa_fwd_ex(q, k, v, causal=causal, q_pos_offset=off, workspace=fresh)
+            for _ in range(3):  # the same stale buffer, call after call
+                got = fa.fa_fwd_ex(q, k, v, causal=causal, q_pos_offset=off, workspace=ws)
+                torch.cuda.synchronize()
+                assert torch.equal(got, want), (B, Hq, Hkv, Sk, D, dtype, kv)
+    assert fa.fa_get_status() == fa.FA_OK
+
+
+def test_decode_replayed_from_a_cuda_graph(fa):
+    """A captured decode launch keeps one flag tag for every replay; the merging CTA clears the
+    flags, so each replay merges all splits again.  New query rows copied in between
+    replays must give the eager result bit for bit."""
+    B, Hq, Hkv, Sk, D = 2, 16, 4, 20000, 128
+    q, k, v = fa_inputs.make_tensors(B, Hq, Hkv, 1, Sk, D, "f16", seed=31, device="cuda")
+    kq, vq = fa.fa_quantize_q4_0(k), fa.fa_quantize_q4_0(v)
+    ws = torch.empty(fa.fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, Sk - 1, True),
+                     dtype=torch.uint8, device="cuda")
+    qs = torch.empty_like(q)
+    os_ = torch.empty_like(q)
+    qs.copy_(q)
+    fa.fa_fwd_ex(qs, kq, vq, os_, causal=True, q_pos_offset=Sk - 1, workspace=ws)  # warm-up
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fa.fa_fwd_ex(qs, kq, vq, os_, causal=True, q_pos_offset=Sk - 1, workspace=ws)
+    for seed in (1, 2, 3, 4):
+        qn = torch.randn(q.shape, generator=torch.Generator(device="cuda").manual_seed(seed),
+                         device="cuda").to(q.dtype)
+        qs.copy_(qn)
+        graph.replay()
+        torch.cuda.synchronize()
+        want = fa.fa_fwd_ex(qn, kq, vq, causal=True, q_pos_offset=Sk - 1, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(os_, want), seed
+    assert fa.fa_get_status() == fa.FA_OK
