@@ -378,6 +378,46 @@ def other_legs(fa, dev, stream, flush, peaks):
         ms = time_calls(call, 50, 5, flush=flush, stream=stream)
         tf = w.flops() / (ms * 1e-3) / 1e12
         out[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 2), "frac": round(tf / peak, 4)}
+    # f16 K with a q4_0 V (independent cache formats): 16K chunked prefill and 64K decode
+    w = fa_inputs.WORKLOADS["prefill_gqa32x8_d128_sq2048_sk16384_f16"]
+    q, k, v = fa_inputs.make_qkv(w, device=dev, generate_on_device=True)
+    vq = fa.fa_quantize_q4_0(v)
+    del v
+    o = torch.empty_like(q)
+    ms = time_calls(lambda: fa.fa_fwd_kv(q, k, vq, o, causal=True), 50, 5, flush=flush,
+                    stream=stream)
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    out["prefill_f16k_q4_0v_gqa32x8_d128_sq2048_sk16384"] = {
+        "ms": round(ms, 4), "TFLOP/s": round(tf, 2), "frac": round(tf / peak, 4)}
+    del q, k, vq, o
+    w = fa_inputs.WORKLOADS[DECODE_WORKLOAD]
+    q, k, v = fa_inputs.make_qkv(w, device=dev, generate_on_device=True)
+    vq = fa.fa_quantize_q4_0(v)
+    del v
+    o = torch.empty_like(q)
+    ws = torch.empty(fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset,
+                                           w.causal), dtype=torch.uint8, device=dev)
+    ms = time_calls(lambda: fa.fa_fwd_kv(q, k, vq, o, causal=True, workspace=ws), 100, 5,
+                    stream=stream)
+    keys = w.q_pos_offset + 1
+    nbytes = w.B * w.Hkv * keys * (2 * w.D + w.D // 2 + w.D // 16)
+    out["decode_f16k_q4_0v_b4_gqa32x8_d128_sk65536"] = {
+        "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "kv_bytes_per_call": nbytes}
+    del q, k, vq, o
+    # append a 16K-token chunk of K and V (B 4, 8 kv heads) into q4_0 caches of 64K tokens
+    w = fa_inputs.WORKLOADS[DECODE_WORKLOAD]
+    kn = torch.randn(w.B, w.Hkv, 16384, w.D, device=dev).to(torch.float16)
+    vn = torch.randn_like(kn)
+    kc, vc = fa.q4_0_cache(w.B, w.Hkv, w.Sk, w.D), fa.q4_0_cache(w.B, w.Hkv, w.Sk, w.D)
+    ms = time_calls(lambda: fa.fa_append_q4_0(kn, kc, 32768, vn, vc), 20, 3, stream=stream)
+    rows = 2 * w.B * w.Hkv * 16384
+    nbytes = rows * (w.D * 2 + w.D // 2 + w.D // 16)
+    out["append_q4_0_kv_b4_h8_d128_chunk16384"] = {
+        "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    del kn, vn, kc, vc
     # q4_0 cache build: reads f16 K (D*2 B per row), writes D/2 + D/16 B per row
     w = fa_inputs.WORKLOADS[DECODE_WORKLOAD]
     _, k, _ = fa_inputs.make_qkv(w, device=dev, generate_on_device=True)

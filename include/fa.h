@@ -95,6 +95,23 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
                     fa_dtype dtype, fa_kv_format kv_format, void* workspace,
                     size_t workspace_bytes, int32_t* rescale_count, fa_stream_t stream);
 
+/* fa_fwd_ex over K/V caches with independent formats and a token capacity.
+ * The cache configuration "FlashAttention on gfx90a: Why It's Broken and How to Fix It" (The V
+ * Dequantization Gap; Impact of the V Dequant Patch) describes users being pushed into -- f16 K
+ * with a q4_0 V, set separately with -ctk / -ctv -- and the chunked-prefill flow where a chunk
+ * attends to a cache that is larger than the tokens filled so far.
+ *  k, v       : [B, Hkv, kv_capacity, D] each, in its own format: k_format / v_format (dense in
+ *               the dtype of Q, or a q4_0 tensor built for [B, Hkv, kv_capacity, D]);
+ *               only tokens 0 .. Sk - 1 of each (batch, kv head) are read
+ *  kv_capacity: >= Sk (the cache's allocated length; Sk = tokens filled)
+ *  Other arguments, scratch, errors: as fa_fwd_ex (fa_workspace_bytes covers every pair of
+ *  formats).  fa_fwd_ex(…) is fa_fwd_kv with k_format = v_format and kv_capacity = Sk. */
+fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                    int Sq, int Sk, int kv_capacity, int D, int q_pos_offset, int causal,
+                    float scale, fa_dtype dtype, fa_kv_format k_format, fa_kv_format v_format,
+                    void* workspace, size_t workspace_bytes, int32_t* rescale_count,
+                    fa_stream_t stream);
+
 /* Scratch bytes fa_fwd_ex needs for this shape (0 for Sq >= 2). */
 size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
                           int causal);
@@ -138,6 +155,20 @@ size_t fa_q4_0_scale_offset(int B, int H, int S, int D);
 fa_status fa_quantize_q4_0(const void* x, void* out_q4, int B, int H, int S, int D,
                            fa_dtype dtype, fa_stream_t stream);
 
+/* Append a chunk of new tokens to q4_0 caches: quantizes k_new (and v_new, in the same launch)
+ * straight into tokens pos0 .. pos0 + S_new - 1 of each (batch, head) of k_cache (v_cache), with
+ * the bits fa_quantize_q4_0 would produce.  This is the step before a chunked prefill over a
+ * q4_0 cache ("FlashAttention on gfx90a: Why It's Broken and How to Fix It", Impact of the V
+ * Dequant Patch: the cache is stored quantized).
+ *  k_new, v_new     : [B, H, S_new, D] in `dtype`, device memory; v_new may be NULL (then
+ *                     v_cache must be NULL too)
+ *  k_cache, v_cache : q4_0 tensors of fa_q4_0_bytes(B, H, kv_capacity, D) bytes
+ *  Requires 0 <= pos0, pos0 + S_new <= kv_capacity, D % 32 == 0; tokens outside the range are
+ *  left untouched.  Inputs must be finite. */
+fa_status fa_append_q4_0(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         int B, int H, int S_new, int kv_capacity, int pos0, int D,
+                         fa_dtype dtype, fa_stream_t stream);
+
 /* Synchronize `stream`, then report (and clear) any device-side error recorded by this
  * library's kernels since the last call: FA_ERR_TIMEOUT when a bounded wait inside a kernel ran
  * out (the kernel then abandoned its work and returned), FA_ERR_CUDA when the stream reports a
@@ -153,7 +184,7 @@ const char* fa_status_string(fa_status s);
  * or hang is involved. */
 fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 101 adds fa_fwd_kv and fa_append_q4_0. */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -25,7 +25,7 @@ FA_KV_DENSE, FA_KV_Q4_0 = 0, 1
 EXPORTED = (
     "fa_fwd", "fa_fwd_ex", "fa_workspace_bytes", "fa_q4_0_bytes", "fa_q4_0_scale_offset",
     "fa_quantize_q4_0", "fa_get_status", "fa_status_string", "fa_debug_wait_timeout",
-    "fa_version", "fa_fwd_decode_noalloc",
+    "fa_version", "fa_fwd_decode_noalloc", "fa_fwd_kv", "fa_append_q4_0",
 )
 
 _lib = None
@@ -79,6 +79,11 @@ def load_from(p: str) -> ctypes.CDLL:
     lib.fa_version.restype = i
     lib.fa_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_decode_noalloc.restype = i
+    lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, i, vp, sz, vp,
+                              vp]
+    lib.fa_fwd_kv.restype = i
+    lib.fa_append_q4_0.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+    lib.fa_append_q4_0.restype = i
     return lib
 
 
@@ -260,3 +265,89 @@ def fa_fwd_decode_noalloc(q, k, v, o=None, *, causal: bool = True,
         raise ValueError("fa_fwd_decode_noalloc takes one query token per sequence (Sq == 1)")
     _check(lib.fa_fwd_decode_noalloc(*a[:7], *a[8:], _stream(stream)), "fa_fwd_decode_noalloc")
     return o
+
+
+def _side(t):
+    """(format code, [B, H, S, D]) of one K or V operand: a dense tensor or a Q4Tensor."""
+    if isinstance(t, Q4Tensor):
+        return FA_KV_Q4_0, tuple(t.shape)
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError("dense k/v must be contiguous [B, Hkv, S, D] tensors")
+    return FA_KV_DENSE, tuple(t.shape)
+
+
+def fa_fwd_kv(q, k, v, o=None, *, Sk: int | None = None, causal: bool = True,
+              q_pos_offset: int | None = None, scale: float | None = None,
+              workspace: torch.Tensor | None = None, rescale_count: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """Attention over K/V caches whose formats are chosen independently (each a dense tensor in
+    q's dtype or a Q4Tensor) and whose token capacity (their third dimension) may exceed the Sk
+    tokens filled (default: the capacity).  q_pos_offset defaults to Sk - Sq."""
+    if o is None:
+        o = torch.empty_like(q)
+    if q.dim() != 4 or not q.is_contiguous() or not o.is_contiguous() or o.shape != q.shape:
+        raise ValueError("q and o must be contiguous [B, Hq, Sq, D] tensors of the same shape")
+    kf, (Bk, Hkv, Scap, Dk) = _side(k)
+    vf, vshape = _side(v)
+    if vshape != (Bk, Hkv, Scap, Dk):
+        raise ValueError("k and v must have the same [B, Hkv, capacity, D]")
+    B, Hq, Sq, D = q.shape
+    if Bk != B or Dk != D:
+        raise ValueError("k/v batch or head dim does not match q")
+    for t, f in ((k, kf), (v, vf)):
+        if f == FA_KV_DENSE and t.dtype != q.dtype:
+            raise TypeError("dense k/v must have the dtype of q")
+    Sk = Scap if Sk is None else int(Sk)
+    if q_pos_offset is None:
+        q_pos_offset = Sk - Sq
+    if scale is None:
+        scale = D ** -0.5
+    lib = load()
+    if workspace is None:
+        need = lib.fa_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, int(q_pos_offset), int(bool(causal)))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc_ptr = None
+    if rescale_count is not None:
+        if rescale_count.dtype != torch.int32 or rescale_count.numel() != B * Hq * Sq:
+            raise ValueError("rescale_count must be int32 [B, Hq, Sq]")
+        rc_ptr = rescale_count.data_ptr()
+    _check(lib.fa_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq,
+                         Sk, Scap, D, int(q_pos_offset), int(bool(causal)), float(scale),
+                         _dtype_code(q.dtype), kf, vf, ws_ptr, ws_bytes, rc_ptr, _stream(stream)),
+           "fa_fwd_kv")
+    return o
+
+
+def q4_0_cache(B: int, H: int, capacity: int, D: int, device="cuda") -> Q4Tensor:
+    """An empty (uninitialised) q4_0 cache of logical shape [B, H, capacity, D]."""
+    nbytes = fa_q4_0_bytes(B, H, capacity, D)
+    if nbytes == 0:
+        raise ValueError("D must be a positive multiple of 32")
+    return Q4Tensor(torch.empty(nbytes, dtype=torch.uint8, device=device), B, H, capacity, D)
+
+
+def fa_append_q4_0(k_new: torch.Tensor, k_cache: Q4Tensor, pos0: int,
+                   v_new: torch.Tensor | None = None, v_cache: Q4Tensor | None = None, *,
+                   stream=None) -> None:
+    """Quantize k_new (and v_new) [B, H, S_new, D] into tokens pos0 .. pos0 + S_new - 1 of the
+    q4_0 caches, in one launch."""
+    if k_new.dim() != 4 or not k_new.is_contiguous():
+        raise ValueError("k_new must be a contiguous [B, H, S_new, D] tensor")
+    B, H, S_new, D = k_new.shape
+    if (k_cache.B, k_cache.H, k_cache.D) != (B, H, D):
+        raise ValueError("k_cache does not match k_new")
+    if (v_new is None) != (v_cache is None):
+        raise ValueError("give both v_new and v_cache, or neither")
+    if v_new is not None:
+        if tuple(v_new.shape) != tuple(k_new.shape) or not v_new.is_contiguous():
+            raise ValueError("v_new must match k_new")
+        if v_cache.shape != k_cache.shape:
+            raise ValueError("v_cache must match k_cache")
+    _check(load().fa_append_q4_0(k_new.data_ptr(), v_new.data_ptr() if v_new is not None else None,
+                                 k_cache.data_ptr(),
+                                 v_cache.data_ptr() if v_cache is not None else None, B, H, S_new,
+                                 k_cache.S, int(pos0), D, _dtype_code(k_new.dtype),
+                                 _stream(stream)), "fa_append_q4_0")

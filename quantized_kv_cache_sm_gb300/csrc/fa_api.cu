@@ -63,6 +63,16 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// map of a K or V tensor [BHkv][Scap][D]: q4_0 nibble tiles (D/2 bytes x `tile` keys, 64-B or
+// 32-B swizzle) or dense tiles (64 elements x `tile` keys, 128-B swizzle)
+bool kv_map(CUtensorMap* m, const void* base, bool q4, CUtensorMapDataType tdt, int D, int Scap,
+            uint64_t BHkv, uint32_t tile, CUtensorMapSwizzle nib_sw) {
+  if (q4)
+    return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Scap, BHkv, D / 2, tile,
+                    nib_sw);
+  return make_map(m, base, tdt, 2, D, Scap, BHkv, 64, tile, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int num_sms() {
@@ -95,13 +105,13 @@ fa_status check_common(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_
   return FA_OK;
 }
 
-// decode scratch of one cache format (0 for Sq >= 2)
+// decode scratch of one pair of cache formats (0 for Sq >= 2)
 size_t workspace_for(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
-                     int causal, bool q4, int* nsplit_out, int* chunk_out) {
+                     int causal, bool kq4, bool vq4, int* nsplit_out, int* chunk_out) {
   if (Sq != 1) return 0;
   const int sk_eff = causal ? q_pos_offset + 1 : Sk;
   int ns = 1, ck = sk_eff;
-  decode_plan(B, Hkv, sk_eff, num_sms(), q4, &ns, &ck);
+  decode_plan(B, Hkv, sk_eff, num_sms(), kq4, vq4, &ns, &ck);
   if (nsplit_out) *nsplit_out = ns;
   if (chunk_out) *chunk_out = ck;
   return decode_flag_bytes(B, Hkv, ns) +
@@ -122,14 +132,16 @@ uint32_t next_call_tag() {
   return t ? t : 1u;
 }
 
-// enough decode scratch for either cache format
+// enough decode scratch for any pair of cache formats
 size_t workspace_any(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
                      int causal) {
-  const size_t a = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, true, nullptr,
-                                 nullptr);
-  const size_t b = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, false, nullptr,
-                                 nullptr);
-  return a > b ? a : b;
+  size_t m = 0;
+  for (int f = 0; f < 3; ++f) {  // both q4_0, both dense, one of each (one plan for either)
+    const size_t w = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, f != 1, f == 0,
+                                   nullptr, nullptr);
+    if (w > m) m = w;
+  }
+  return m;
 }
 
 }  // namespace
@@ -165,51 +177,70 @@ fa_status fa_quantize_q4_0(const void* x, void* out_q4, int B, int H, int S, int
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
   const int64_t rows = static_cast<int64_t>(B) * H * S;
   uint8_t* base = static_cast<uint8_t*>(out_q4);
-  const cudaError_t e = quantize_launch(x, base, base + q4_scale_offset(rows, D), rows, D,
+  const QuantJob j0 = {x, base, base + q4_scale_offset(rows, D)};
+  const QuantJob none = {nullptr, nullptr, nullptr};
+  const cudaError_t e = quantize_launch(j0, none, static_cast<int64_t>(B) * H, S, S, 0, D,
                                         dtype == FA_BF16, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
-                    int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
-                    fa_dtype dtype, fa_kv_format kv_format, void* workspace,
-                    size_t workspace_bytes, int32_t* rescale_count, fa_stream_t stream) {
+fa_status fa_append_q4_0(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         int B, int H, int S_new, int kv_capacity, int pos0, int D,
+                         fa_dtype dtype, fa_stream_t stream) {
+  if (!aligned16(k_new) || !aligned16(k_cache)) return FA_ERR_INVALID_ARG;
+  if ((v_new == nullptr) != (v_cache == nullptr)) return FA_ERR_INVALID_ARG;
+  if (v_new && (!aligned16(v_new) || !aligned16(v_cache))) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S_new < 1 || kv_capacity < 1 || D < 32 || D % 32)
+    return FA_ERR_INVALID_ARG;
+  if (pos0 < 0 || static_cast<int64_t>(pos0) + S_new > kv_capacity) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const size_t soff = q4_scale_offset(BH * kv_capacity, D);
+  uint8_t* kc = static_cast<uint8_t*>(k_cache);
+  uint8_t* vc = static_cast<uint8_t*>(v_cache);
+  const QuantJob jk = {k_new, kc, kc + soff};
+  const QuantJob jv = {v_new, vc, vc ? vc + soff : nullptr};
+  const cudaError_t e = quantize_launch(jk, jv, BH, S_new, kv_capacity, pos0, D,
+                                        dtype == FA_BF16, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                    int Sq, int Sk, int kv_capacity, int D, int q_pos_offset, int causal,
+                    float scale, fa_dtype dtype, fa_kv_format k_format, fa_kv_format v_format,
+                    void* workspace, size_t workspace_bytes, int32_t* rescale_count,
+                    fa_stream_t stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
-  const fa_status st =
-      check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale, dtype, kv_format);
+  fa_status st = check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale, dtype, k_format);
   if (st != FA_OK) return st;
+  if (v_format != FA_KV_DENSE && v_format != FA_KV_Q4_0) return FA_ERR_INVALID_ARG;
+  if (kv_capacity < Sk) return FA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * Hkv * kv_capacity * D >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  const int Scap = kv_capacity;
   const bool bf16 = dtype == FA_BF16;
-  const bool q4 = kv_format == FA_KV_Q4_0;
+  const bool kq4 = k_format == FA_KV_Q4_0;
+  const bool vq4 = v_format == FA_KV_Q4_0;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const CUtensorMapDataType tdt =
       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const uint64_t BHkv = static_cast<uint64_t>(B) * Hkv;
-  const size_t kv_scale_off = q4 ? q4_scale_offset(static_cast<int64_t>(BHkv) * Sk, D) : 0;
+  const size_t kv_scale_off = q4_scale_offset(static_cast<int64_t>(BHkv) * Scap, D);
   const CUtensorMapSwizzle nib_sw =
       D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 
   if (Sq == 1) {
     int nsplit = 1, chunk = 1;
     const size_t need =
-        workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, q4, &nsplit, &chunk);
-    const uint32_t tile = static_cast<uint32_t>(decode_tile_keys(q4));
+        workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, kq4, vq4, &nsplit, &chunk);
+    const uint32_t tile = static_cast<uint32_t>(decode_tile_keys(kq4, vq4));
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
       return FA_ERR_INVALID_ARG;
     DecodeLaunch L;
-    bool ok;
-    if (q4) {
-      ok = make_map(&L.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, tile,
-                    nib_sw) &&
-           make_map(&L.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, tile,
-                    nib_sw);
-      L.k_scale = static_cast<const uint8_t*>(k) + kv_scale_off;
-      L.v_scale = static_cast<const uint8_t*>(v) + kv_scale_off;
-    } else {
-      ok = make_map(&L.tm_k, k, tdt, 2, D, Sk, BHkv, 64, tile, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_map(&L.tm_v, v, tdt, 2, D, Sk, BHkv, 64, tile, CU_TENSOR_MAP_SWIZZLE_128B);
-      L.k_scale = L.v_scale = nullptr;
-    }
-    if (!ok) return FA_ERR_CUDA;
+    if (!kv_map(&L.tm_k, k, kq4, tdt, D, Scap, BHkv, tile, nib_sw) ||
+        !kv_map(&L.tm_v, v, vq4, tdt, D, Scap, BHkv, tile, nib_sw))
+      return FA_ERR_CUDA;
+    L.k_scale = kq4 ? static_cast<const uint8_t*>(k) + kv_scale_off : nullptr;
+    L.v_scale = vq4 ? static_cast<const uint8_t*>(v) + kv_scale_off : nullptr;
     L.q = q;
     L.o = o;
     L.flags = static_cast<uint32_t*>(workspace);
@@ -220,33 +251,26 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
     L.Hq = Hq;
     L.Hkv = Hkv;
     L.Sk = Sk;
+    L.Scap = Scap;
     L.Sk_eff = causal ? q_pos_offset + 1 : Sk;
     L.D = D;
     L.nsplit = nsplit;
     L.chunk = chunk;
     L.scale = scale;
     L.bf16 = bf16;
-    L.q4 = q4;
+    L.kq4 = kq4;
+    L.vq4 = vq4;
     return decode_launch(L, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
 
   PrefillLaunch L;
-  bool ok = make_map(&L.tm_q, q, tdt, 2, D, Sq, static_cast<uint64_t>(B) * Hq, 64, 128,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-  if (q4) {
-    ok = ok &&
-         make_map(&L.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, 128,
-                  nib_sw) &&
-         make_map(&L.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D / 2, Sk, BHkv, D / 2, 128,
-                  nib_sw);
-    L.k_scale = static_cast<const uint8_t*>(k) + kv_scale_off;
-    L.v_scale = static_cast<const uint8_t*>(v) + kv_scale_off;
-  } else {
-    ok = ok && make_map(&L.tm_k, k, tdt, 2, D, Sk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_map(&L.tm_v, v, tdt, 2, D, Sk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-    L.k_scale = L.v_scale = nullptr;
-  }
-  if (!ok) return FA_ERR_CUDA;
+  if (!make_map(&L.tm_q, q, tdt, 2, D, Sq, static_cast<uint64_t>(B) * Hq, 64, 128,
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !kv_map(&L.tm_k, k, kq4, tdt, D, Scap, BHkv, 128, nib_sw) ||
+      !kv_map(&L.tm_v, v, vq4, tdt, D, Scap, BHkv, 128, nib_sw))
+    return FA_ERR_CUDA;
+  L.k_scale = kq4 ? static_cast<const uint8_t*>(k) + kv_scale_off : nullptr;
+  L.v_scale = vq4 ? static_cast<const uint8_t*>(v) + kv_scale_off : nullptr;
   L.o = o;
   L.rescale_count = rescale_count;
   L.B = B;
@@ -254,13 +278,23 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
   L.Hkv = Hkv;
   L.Sq = Sq;
   L.Sk = Sk;
+  L.Scap = Scap;
   L.D = D;
   L.q_pos_offset = causal ? q_pos_offset : 0;
   L.causal = causal ? 1 : 0;
   L.scale = scale;
   L.bf16 = bf16;
-  L.q4 = q4;
+  L.kq4 = kq4;
+  L.vq4 = vq4;
   return prefill_launch(L, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                    int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
+                    fa_dtype dtype, fa_kv_format kv_format, void* workspace,
+                    size_t workspace_bytes, int32_t* rescale_count, fa_stream_t stream) {
+  return fa_fwd_kv(q, k, v, o, B, Hq, Hkv, Sq, Sk, Sk, D, q_pos_offset, causal, scale, dtype,
+                   kv_format, kv_format, workspace, workspace_bytes, rescale_count, stream);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
@@ -271,8 +305,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, in
       check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale, dtype, kv_format);
   if (st != FA_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t need = workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal,
-                                    kv_format == FA_KV_Q4_0, nullptr, nullptr);
+  const bool q4 = kv_format == FA_KV_Q4_0;
+  const size_t need =
+      workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, q4, q4, nullptr, nullptr);
   void* ws = nullptr;
   if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess) return FA_ERR_CUDA;
   const fa_status r = fa_fwd_ex(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale,
@@ -315,6 +350,6 @@ fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream) {
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 101; }
 
 }  // extern "C"

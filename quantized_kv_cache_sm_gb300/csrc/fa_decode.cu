@@ -1,4 +1,4 @@
-// Split-K decode (one query token per sequence) for sm_103a, dense or q4_0 K/V cache.
+// Split-K decode (one query token per sequence) for sm_103a; K and V each dense or q4_0.
 //
 // Decode reads the whole K/V cache once per token, so it is bound by HBM bandwidth, not by the
 // tensor cores (the pages' decode figures, "FlashAttention on gfx90a: Why It's Broken and How to
@@ -37,9 +37,10 @@ namespace {
 constexpr int kConsumers = 4;  // consumer warps per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, bool Q4>
+template <int D, bool KQ4, bool VQ4>
 struct DCfg {
-  static constexpr int kSub = Q4 ? 2 : 1;                      // 16-key sub-tiles per warp step
+  static constexpr bool kAnyQ4 = KQ4 || VQ4;
+  static constexpr int kSub = kAnyQ4 ? 2 : 1;                  // 16-key sub-tiles per warp step
   static constexpr int kTileKeys = 16 * kSub * kConsumers;     // keys per stage
   static constexpr int kNB = D / 32;                           // q4_0 blocks per key row
   static constexpr int kRow = kNB * 2;                         // scale bytes per key row
@@ -49,14 +50,16 @@ struct DCfg {
   // 2); V as f32 [key][block] (bf16) or as fp16 key pairs [16-key group][t][half][block] (f16)
   static constexpr int kScaleBytes = kTileKeys * kNB * 4;
   static constexpr int kDenseBytes = kTileKeys * D * 2;
-  static constexpr int kKBytes = Q4 ? kNibBytes : kDenseBytes;
-  // stage: K tile | V tile | K scales | V scales
+  static constexpr int kKBytes = KQ4 ? kNibBytes : kDenseBytes;
+  static constexpr int kVBytes = VQ4 ? kNibBytes : kDenseBytes;
+  // stage: K tile | V tile | K scales (q4_0 K) | V scales (q4_0 V)
   static constexpr int kOffV = (kKBytes + 1023) / 1024 * 1024;
-  static constexpr int kOffKs = kOffV + (kKBytes + 1023) / 1024 * 1024;
-  static constexpr int kOffVs = kOffKs + (Q4 ? kScaleBytes : 0);
-  static constexpr int kStageBytes = ((kOffVs + (Q4 ? kScaleBytes : 0)) + 1023) / 1024 * 1024;
-  static constexpr int kStages = Q4 ? (D == 128 ? 3 : 6) : (D == 128 ? 3 : 6);
-  static constexpr int kCtasPerSm = Q4 ? 3 : 2;
+  static constexpr int kOffKs = kOffV + (kVBytes + 1023) / 1024 * 1024;
+  static constexpr int kOffVs = kOffKs + (KQ4 ? kScaleBytes : 0);
+  static constexpr int kStageBytes = ((kOffVs + (VQ4 ? kScaleBytes : 0)) + 1023) / 1024 * 1024;
+  // one dense side of 128 keys makes a stage ~42 KB (D = 128): two stages and two CTAs per SM
+  static constexpr int kStages = (KQ4 == VQ4) ? (D == 128 ? 3 : 6) : (D == 128 ? 2 : 4);
+  static constexpr int kCtasPerSm = (KQ4 && VQ4) ? 3 : 2;
   static constexpr int kOffBar = kStages * kStageBytes;
   static constexpr int kOffQ = kOffBar + 256;  // the group's query rows, [8][D] 16-bit
   static constexpr int kSmemBytes = kOffQ + 8 * D * 2 + 1024;
@@ -180,6 +183,7 @@ struct DecodeArgs {
   const uint8_t* k_scale;
   const uint8_t* v_scale;
   float* partial;
+  int Scap;  // tokens per (batch, kv head) in the K/V tensors (row stride); Sk <= Scap
   // arrival flags [B, Hkv, nsplit]: a split that has published its partials stores this call's
   // tag in its flag.  A flag holding anything else counts as not arrived, so the workspace needs
   // no clearing; a merging CTA sets its flags back to 0, so a replay of the same launch (same
@@ -190,11 +194,12 @@ struct DecodeArgs {
   float scale_log2;
 };
 
-template <int D, bool BF16, bool Q4>
-__global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm)
+template <int D, bool BF16, bool KQ4, bool VQ4>
+__global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs args) {
-  using C = DCfg<D, Q4>;
+  using C = DCfg<D, KQ4, VQ4>;
+  constexpr bool Q4 = C::kAnyQ4;  // some side streams q4_0 (scale rows through the producer)
   constexpr int kSub = C::kSub;
   constexpr int kTileKeys = C::kTileKeys;
   constexpr int kNB = C::kNB;
@@ -247,14 +252,19 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
           const int key = key0 + kKeysPerLane * lane + j;
           kr[j][0] = kr[j][1] = vr[j][0] = vr[j][1] = 0u;
           if (key < args.Sk) {
-            const int64_t off = (bh * args.Sk + key) * C::kRow;
+            const int64_t off = (bh * args.Scap + key) * C::kRow;
             if (kNB == 4) {
-              const uint2 a = __ldg(reinterpret_cast<const uint2*>(args.k_scale + off));
-              const uint2 c = __ldg(reinterpret_cast<const uint2*>(args.v_scale + off));
-              kr[j][0] = a.x; kr[j][1] = a.y; vr[j][0] = c.x; vr[j][1] = c.y;
+              if (KQ4) {
+                const uint2 a = __ldg(reinterpret_cast<const uint2*>(args.k_scale + off));
+                kr[j][0] = a.x; kr[j][1] = a.y;
+              }
+              if (VQ4) {
+                const uint2 c = __ldg(reinterpret_cast<const uint2*>(args.v_scale + off));
+                vr[j][0] = c.x; vr[j][1] = c.y;
+              }
             } else {
-              kr[j][0] = __ldg(reinterpret_cast<const uint32_t*>(args.k_scale + off));
-              vr[j][0] = __ldg(reinterpret_cast<const uint32_t*>(args.v_scale + off));
+              if (KQ4) kr[j][0] = __ldg(reinterpret_cast<const uint32_t*>(args.k_scale + off));
+              if (VQ4) vr[j][0] = __ldg(reinterpret_cast<const uint32_t*>(args.v_scale + off));
             }
           }
         }
@@ -268,18 +278,22 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
       }
       const uint32_t st = sbase + s * C::kStageBytes;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_full + 8 * s, 2 * C::kKBytes);
-        if constexpr (Q4) {
+        mbar_arrive_expect_tx(bar_full + 8 * s, C::kKBytes + C::kVBytes);
+        if constexpr (KQ4) {
           tma_load_3d(st, &tm_k, bar_full + 8 * s, 0, key0, static_cast<int>(bh));
+        } else {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(st + c * (kTileKeys * 128), &tm_k, bar_full + 8 * s, 64 * c, key0,
+                        static_cast<int>(bh));
+        }
+        if constexpr (VQ4) {
           tma_load_3d(st + C::kOffV, &tm_v, bar_full + 8 * s, 0, key0, static_cast<int>(bh));
         } else {
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d(st + c * (kTileKeys * 128), &tm_k, bar_full + 8 * s, 64 * c, key0,
-                        static_cast<int>(bh));
+          for (int c = 0; c < D / 64; ++c)
             tma_load_3d(st + C::kOffV + c * (kTileKeys * 128), &tm_v, bar_full + 8 * s, 64 * c,
                         key0, static_cast<int>(bh));
-          }
         }
       }
       if constexpr (Q4) {
@@ -287,18 +301,20 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
 #pragma unroll
         for (int j = 0; j < kKeysPerLane; ++j) {
           const int kt = kKeysPerLane * lane + j;  // key within the tile
-          float kf[kNB];
+          if (KQ4) {
+            float kf[kNB];
 #pragma unroll
-          for (int blk = 0; blk < kNB; ++blk)
-            kf[blk] = __half2float(__ushort_as_half(
-                          static_cast<uint16_t>(kr[j][blk >> 1] >> (16 * (blk & 1))))) *
-                      args.scale_log2;
-          float* kdst = reinterpret_cast<float*>(stg + C::kOffKs) + kt * kNB;
-          if (kNB == 4)
-            *reinterpret_cast<float4*>(kdst) = make_float4(kf[0], kf[1], kf[2], kf[3]);
-          else
-            *reinterpret_cast<float2*>(kdst) = make_float2(kf[0], kf[1]);
-          if (BF16) {
+            for (int blk = 0; blk < kNB; ++blk)
+              kf[blk] = __half2float(__ushort_as_half(
+                            static_cast<uint16_t>(kr[j][blk >> 1] >> (16 * (blk & 1))))) *
+                        args.scale_log2;
+            float* kdst = reinterpret_cast<float*>(stg + C::kOffKs) + kt * kNB;
+            if (kNB == 4)
+              *reinterpret_cast<float4*>(kdst) = make_float4(kf[0], kf[1], kf[2], kf[3]);
+            else
+              *reinterpret_cast<float2*>(kdst) = make_float2(kf[0], kf[1]);
+          }
+          if (BF16 && VQ4) {
             float vf[kNB];
 #pragma unroll
             for (int blk = 0; blk < kNB; ++blk)
@@ -311,7 +327,7 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
               *reinterpret_cast<float2*>(vdst) = make_float2(vf[0], vf[1]);
           }
         }
-        if (!BF16) {
+        if (!BF16 && VQ4) {
           // key pairs (4*lane, 4*lane+1) and (4*lane+2, 4*lane+3): fp16 pairs per block at
           // [16-key group][t][half][block], t and half from the pair's position in its group
 #pragma unroll
@@ -371,7 +387,7 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       int d[4];
-      if (Q4) {
+      if (KQ4) {
         d[0] = 16 * kk + 4 * t4;
         d[1] = d[0] + 2;
         d[2] = d[0] + 1;
@@ -386,13 +402,13 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         uint16_t v = valid ? qrow[d[i]] : static_cast<uint16_t>(0);
-        if (Q4 && !BF16 && (kk & 1)) v = f2h<false>(h2f<false>(v) * 0.0625f);
+        if (KQ4 && !BF16 && (kk & 1)) v = f2h<false>(h2f<false>(v) * 0.0625f);
         e[i] = v;
       }
       qf[kk][0] = e[0] | (e[1] << 16);
       qf[kk][1] = e[2] | (e[3] << 16);
     }
-    if constexpr (Q4) {
+    if constexpr (KQ4) {
 #pragma unroll
       for (int blk = 0; blk < kNB; ++blk) {
 #pragma unroll
@@ -435,7 +451,7 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
     for (int u = 0; u < kSub; ++u) {
       const int kl = (kSub * 16) * cw + 16 * u;  // first key of the sub-tile in the stage
       sc[u][0] = sc[u][1] = sc[u][2] = sc[u][3] = 0.f;
-      if constexpr (Q4) {
+      if constexpr (KQ4) {
         float kf_g[4], kf_g8[4];  // f32 scales (times the base-2 softmax scale), keys g, g+8
         if (kNB == 4) {
           const uint4 x = lds128(st + C::kOffKs + (kl + g8) * 16);
@@ -504,7 +520,7 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
 #pragma unroll
     for (int u = 0; u < kSub; ++u) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) t[u][i] = Q4 ? sc[u][i] : sc[u][i] * sl2;
+      for (int i = 0; i < 4; ++i) t[u][i] = KQ4 ? sc[u][i] : sc[u][i] * sl2;
       if (!full_tile) {
         const int keyg = tile_key0 + (kSub * 16) * cw + 16 * u + g8;
         if (keyg >= kb1) t[u][0] = t[u][1] = -INFINITY;
@@ -550,7 +566,7 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
 #pragma unroll
     for (int u = 0; u < kSub; ++u) {
       const int kl = (kSub * 16) * cw + 16 * u;
-      if constexpr (Q4) {
+      if constexpr (VQ4) {
         const uint32_t vbase = st + C::kOffV;
         // P of keys (2t, 2t+1) and (2t+8, 2t+9) for head g (f16: transposed once, then scaled
         // per block with the V scales of those key pairs)
@@ -660,7 +676,7 @@ __global__ void __launch_bounds__(DCfg<D, Q4>::kThreads, DCfg<D, Q4>::kCtasPerSm
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) {
       int dr0, dr1;  // head-dim rows of accumulator rows g and g+8 of m-tile i
-      if (Q4) {
+      if (VQ4) {
         dr0 = 32 * (i >> 1) + 16 * (i & 1) + 2 * g8;
         dr1 = dr0 + 1;
       } else {
@@ -801,15 +817,22 @@ size_t decode_flag_bytes(int B, int Hkv, int nsplit) {
   return (static_cast<size_t>(B) * Hkv * nsplit * sizeof(uint32_t) + 255) / 256 * 256;
 }
 
-int decode_tile_keys(bool q4) {
-  return q4 ? DCfg<128, true>::kTileKeys : DCfg<128, false>::kTileKeys;
+int decode_tile_keys(bool kq4, bool vq4) {
+  return (kq4 || vq4) ? DCfg<128, true, true>::kTileKeys : DCfg<128, false, false>::kTileKeys;
 }
 
-void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool q4, int* nsplit, int* chunk) {
+static int decode_ctas_per_sm(bool kq4, bool vq4) {
+  if (kq4 && vq4) return DCfg<128, true, true>::kCtasPerSm;
+  if (kq4 || vq4) return DCfg<128, true, false>::kCtasPerSm;
+  return DCfg<128, false, false>::kCtasPerSm;
+}
+
+void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool kq4, bool vq4, int* nsplit,
+                 int* chunk) {
   // one wave of CTAs at the kernel's resident count, equal key chunks of whole tiles
-  const int tile = decode_tile_keys(q4);
+  const int tile = decode_tile_keys(kq4, vq4);
   const int units = B * Hkv;
-  const int slots = num_sms * (q4 ? DCfg<128, true>::kCtasPerSm : DCfg<128, false>::kCtasPerSm);
+  const int slots = num_sms * decode_ctas_per_sm(kq4, vq4);
   int ns = slots / units;
   if (ns < 1) ns = 1;
   const int max_tiles = (Sk_eff + tile - 1) / tile;
@@ -822,10 +845,10 @@ void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool q4, int* nsplit, 
   *nsplit = (Sk_eff + ck - 1) / ck;
 }
 
-template <int D, bool BF16, bool Q4>
+template <int D, bool BF16, bool KQ4, bool VQ4>
 static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
-  using C = DCfg<D, Q4>;
-  auto kern = decode_split_kernel<D, BF16, Q4>;
+  using C = DCfg<D, KQ4, VQ4>;
+  auto kern = decode_split_kernel<D, BF16, KQ4, VQ4>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -835,6 +858,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   a.v_scale = static_cast<const uint8_t*>(L.v_scale);
   a.o = static_cast<uint16_t*>(L.o);
   a.partial = L.partial;
+  a.Scap = L.Scap;
   a.flags = L.flags;
   a.tag = L.tag;
   a.Hq = L.Hq;
@@ -849,13 +873,18 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int D, bool BF16>
+static cudaError_t launch_fmt(const DecodeLaunch& L, cudaStream_t stream) {
+  if (L.kq4) return L.vq4 ? launch_t<D, BF16, true, true>(L, stream)
+                          : launch_t<D, BF16, true, false>(L, stream);
+  return L.vq4 ? launch_t<D, BF16, false, true>(L, stream)
+               : launch_t<D, BF16, false, false>(L, stream);
+}
+
 cudaError_t decode_launch(const DecodeLaunch& L, cudaStream_t stream) {
-  if (L.D == 128) {
-    if (L.q4) return L.bf16 ? launch_t<128, true, true>(L, stream) : launch_t<128, false, true>(L, stream);
-    return L.bf16 ? launch_t<128, true, false>(L, stream) : launch_t<128, false, false>(L, stream);
-  }
-  if (L.q4) return L.bf16 ? launch_t<64, true, true>(L, stream) : launch_t<64, false, true>(L, stream);
-  return L.bf16 ? launch_t<64, true, false>(L, stream) : launch_t<64, false, false>(L, stream);
+  if (L.D == 128)
+    return L.bf16 ? launch_fmt<128, true>(L, stream) : launch_fmt<128, false>(L, stream);
+  return L.bf16 ? launch_fmt<64, true>(L, stream) : launch_fmt<64, false>(L, stream);
 }
 
 uint32_t decode_take_error() {

@@ -8,14 +8,14 @@
 namespace fa {
 
 struct PrefillLaunch {
-  CUtensorMap tm_q, tm_k, tm_v;  // dense: Q/K/V tiles; q4_0: Q tiles and K/V nibble tiles
+  CUtensorMap tm_q, tm_k, tm_v;  // Q tiles; K and V: dense tiles or q4_0 nibble tiles
   void* o;
-  const void* k_scale;           // q4_0 only
-  const void* v_scale;
+  const void* k_scale;           // scale plane of a q4_0 K (else null)
+  const void* v_scale;           // scale plane of a q4_0 V (else null)
   int32_t* rescale_count;
-  int B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal;
+  int B, Hq, Hkv, Sq, Sk, Scap, D, q_pos_offset, causal;  // Scap: K/V tokens per (b, kv head)
   float scale;
-  bool bf16, q4;
+  bool bf16, kq4, vq4;
 };
 cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream);
 uint32_t prefill_take_error();
@@ -29,9 +29,9 @@ struct DecodeLaunch {
   uint32_t* flags;               // [B, Hkv, nsplit] arrival flags (workspace, offset 0)
   float* partial;                // [B, Hq, nsplit, D + 4] f32: m, l, pad, pad, O (workspace)
   uint32_t tag;                  // nonzero, different for every call
-  int B, Hq, Hkv, Sk_eff, Sk, D, nsplit, chunk;
+  int B, Hq, Hkv, Sk_eff, Sk, Scap, D, nsplit, chunk;
   float scale;
-  bool bf16, q4;
+  bool bf16, kq4, vq4;
 };
 cudaError_t decode_launch(const DecodeLaunch& L, cudaStream_t stream);
 uint32_t decode_take_error();
@@ -39,11 +39,19 @@ uint32_t decode_take_error();
 size_t decode_flag_bytes(int B, int Hkv, int nsplit);
 // decode work split for a given shape and cache format (shared by the workspace query and the
 // launch), and the keys per pipeline stage (the TMA box height)
-void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool q4, int* nsplit, int* chunk);
-int decode_tile_keys(bool q4);
+void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool kq4, bool vq4, int* nsplit,
+                 int* chunk);
+int decode_tile_keys(bool kq4, bool vq4);
 
-cudaError_t quantize_launch(const void* x, void* nib, void* scale, int64_t rows, int D, bool bf16,
-                            cudaStream_t stream);
+// q4_0 quantization of up to two tensors in one launch (job 1 may be absent: x1 == nullptr).
+// Source rows [B*H][S_src][D]; row (bh, s) goes to destination row bh * Scap + pos0 + s.
+struct QuantJob {
+  const void* x;
+  void* nib;
+  void* scale;
+};
+cudaError_t quantize_launch(QuantJob j0, QuantJob j1, int64_t BH, int S_src, int Scap, int pos0,
+                            int D, bool bf16, cudaStream_t stream);
 
 cudaError_t debug_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
 uint32_t debug_take_error();

@@ -9,9 +9,9 @@
 //  * one CTA owns two 128-row query tiles (A, B) of one query head; both Q tiles are brought
 //    into shared memory once by TMA and stay there for the CTA's whole key range ("Q is staged
 //    once per block");
-//  * K and V tiles of 128 keys stream through a ring of shared-memory stages, either by TMA
-//    (dense f16/bf16 cache) or as q4_0 nibble/scale tiles that dequant warps expand into the same
-//    f16/bf16 swizzled layout (the fused K and V dequant of "FlashAttention on gfx90a: Why It's
+//  * K and V tiles of 128 keys stream through a ring of shared-memory stages, each side either
+//    by TMA (dense f16/bf16 cache) or as q4_0 nibble/scale tiles that dequant warps expand into
+//    the same f16/bf16 swizzled layout (K and V formats are independent template parameters) (the fused K and V dequant of "FlashAttention on gfx90a: Why It's
 //    Broken and How to Fix It", Why FA-off Can't Do V Quantization, point 5); every K/V tile
 //    serves both query tiles;
 //  * S = Q K^T and O += P V are tcgen05.mma into tensor memory; the single MMA thread
@@ -46,12 +46,16 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM column of the S block of query tile t (0: A, 1: B); P overwrites its first half
 __host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
 
-template <int D, bool Q4>
+template <int D, bool KQ4, bool VQ4>
 struct Cfg {
+  static constexpr bool kAnyQ4 = KQ4 || VQ4;
   static constexpr int kTileBytes = kBN * D * 2;          // one f16/bf16 K or V tile
   static constexpr int kQBytes = kBM * D * 2;             // one Q tile
-  static constexpr int kStages = Q4 ? 3 : (D == 128 ? 4 : 6);
-  static constexpr int kRawStages = Q4 ? 3 : 0;
+  // ring of K/V tiles in MMA order K0 V0 K1 V1 ...; with one q4_0 side the stage count is even,
+  // so K tiles always land on even stages and V tiles on odd ones (fixed arrival counts)
+  static constexpr int kStages = (KQ4 && VQ4) ? 3 : (D == 128 ? 4 : 6);
+  static constexpr int kRawStages = (KQ4 && VQ4) ? 3 : (kAnyQ4 ? 2 : 0);
+  static_assert(KQ4 == VQ4 || kStages % 2 == 0, "mixed formats need an even ring");
   static constexpr int kNibRow = D / 2;                   // bytes of nibbles per key
   static constexpr int kScaleRow = D / 32 * 2;            // bytes of scales per key
   static constexpr int kRawNib = kBN * kNibRow;
@@ -89,6 +93,7 @@ struct PrefillArgs {
   const uint8_t* v_scale;
   int32_t* rescale_count;  // optional [B, Hq, Sq]
   int B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, n_qtiles, n_pairs;
+  int Scap;  // tokens per (batch, kv head) in the K/V tensors (row stride); Sk <= Scap
   float scale_log2;
 };
 
@@ -205,12 +210,12 @@ __device__ __forceinline__ int tile_blocks(const PrefillArgs& a, int q0) {
   return (kend + kBN - 1) / kBN;
 }
 
-template <int D, bool BF16, bool Q4>
-__global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
+template <int D, bool BF16, bool KQ4, bool VQ4>
+__global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
-  using C = Cfg<D, Q4>;
+  using C = Cfg<D, KQ4, VQ4>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -244,7 +249,9 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
     }
     mbar_init(bar(kBarDrain), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(kBarRingFull + s), Q4 ? 64 : 1);  // dequant threads, or the TMA lane
+      // a q4_0 stage is filled by the 64 dequant threads, a dense one by the TMA lane
+      const bool q4s = (C::kStages % 2 == 0) ? ((s & 1) ? VQ4 : KQ4) : (KQ4 && VQ4);
+      mbar_init(bar(kBarRingFull + s), q4s ? 64 : 1);
       mbar_init(bar(kBarRingEmpty + s), 1);
     }
     for (int s = 0; s < C::kRawStages; ++s) {
@@ -278,11 +285,13 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
           tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (kBM * 128), &tm_q,
                       bar(kBarQFull), c * 64, t ? q0B : q0A, b * args.Hq + h);
     }
-    // tiles in the order the MMA first uses them: K0, V0, K1, V1, ...
-    int n = 0;
+    // tiles in the order the MMA first uses them: K0, V0, K1, V1, ...; dense tiles go by TMA
+    // straight into the ring, q4_0 tiles (nibbles + scales) into the raw stages
+    int n = 0;  // ring tiles
+    int r = 0;  // raw q4_0 tiles
     auto produce = [&](bool is_v, int j) {
       if (!ok) return;
-      if constexpr (!Q4) {
+      if (!(is_v ? VQ4 : KQ4)) {
         const int s = n % C::kStages;
         if (lane == 0) {
           if (n >= C::kStages)
@@ -298,10 +307,10 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       } else {
-        const int s = n % C::kRawStages;
-        if (n >= C::kRawStages) {
+        const int s = r % C::kRawStages;
+        if (r >= C::kRawStages) {
           if (lane == 0)
-            ok = mbar_wait(bar(kBarRawEmpty + s), ((n / C::kRawStages) - 1) & 1, abort_flag,
+            ok = mbar_wait(bar(kBarRawEmpty + s), ((r / C::kRawStages) - 1) & 1, abort_flag,
                            &g_prefill_error);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) return;
@@ -318,7 +327,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
           const int key = j * kBN + r;
           const bool in = key < args.Sk;
           const uint8_t* src =
-              sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Sk + (in ? key : 0)) *
+              sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Scap + (in ? key : 0)) *
                        C::kScaleRow;
           const uint32_t d = dst + C::kRawNib + r * C::kScaleRow;
           if (C::kScaleRow == 8)
@@ -327,6 +336,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
             cp_async_4(d, src, in ? 4u : 0u);
         }
         cp_async_mbar_arrive_noinc(bar(kBarRawFull + s));
+        ++r;
       }
       ++n;
     };
@@ -335,13 +345,17 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
       produce(true, j);
     }
     if (!ok && lane == 0) {
-      // let copies already issued land before the CTA's shared memory goes away
+      // let copies already issued land before the CTA's shared memory goes away: the last
+      // dense tiles sent into the ring and the last raw q4_0 tiles
       volatile int never = 0;
-      constexpr int stages = Q4 ? C::kRawStages : C::kStages;
-      for (int i = max(0, n - stages); i < n; ++i) {
-        const int s = i % stages;
-        mbar_wait(bar((Q4 ? kBarRawFull : kBarRingFull) + s), (i / stages) & 1, &never, nullptr,
-                  kWaitLimitNs);
+      for (int i = max(0, n - C::kStages); i < n; ++i)
+        if (!((i & 1) ? VQ4 : KQ4))
+          mbar_wait(bar(kBarRingFull + i % C::kStages), (i / C::kStages) & 1, &never, nullptr,
+                    kWaitLimitNs);
+      if constexpr (C::kAnyQ4) {
+        for (int i = max(0, r - C::kRawStages); i < r; ++i)
+          mbar_wait(bar(kBarRawFull + i % C::kRawStages), (i / C::kRawStages) & 1, &never,
+                    nullptr, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -518,7 +532,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
       if (store && args.rescale_count)
         args.rescale_count[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = nres;
     }
-  } else if constexpr (Q4) {
+  } else if constexpr (C::kAnyQ4) {
     if (warp == 2 || warp == 3) {
       // -------------------------------------------------------------- q4_0 dequant
       // thread u expands key rows u and u + 64 of each raw tile into the 128B-swizzled
@@ -527,10 +541,12 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
       const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
       bool ok = true;
       const int ntiles = 2 * nbmax;
+      int r = 0;  // raw q4_0 tiles consumed
       for (int n = 0; n < ntiles; ++n) {
-        const int rs = n % C::kRawStages;
+        if (!((n & 1) ? VQ4 : KQ4)) continue;  // a dense tile: the producer's TMA fills it
+        const int rs = r % C::kRawStages;
         const int s = n % C::kStages;
-        ok = mbar_wait(bar(kBarRawFull + rs), (n / C::kRawStages) & 1, abort_flag,
+        ok = mbar_wait(bar(kBarRawFull + rs), (r / C::kRawStages) & 1, abort_flag,
                        &g_prefill_error);
         if (ok && n >= C::kStages)
           ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
@@ -585,6 +601,7 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(bar(kBarRingFull + s));
         mbar_arrive(bar(kBarRawEmpty + rs));
+        ++r;
       }
     }
   }
@@ -602,11 +619,11 @@ __global__ void __launch_bounds__(Cfg<D, Q4>::kThreads, 1)
 // ------------------------------------------------------------------------------------------
 // host launch
 // ------------------------------------------------------------------------------------------
-template <int D, bool BF16, bool Q4>
+template <int D, bool BF16, bool KQ4, bool VQ4>
 static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
-  using C = Cfg<D, Q4>;
+  using C = Cfg<D, KQ4, VQ4>;
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
-  auto kern = prefill_kernel<D, BF16, Q4>;
+  auto kern = prefill_kernel<D, BF16, KQ4, VQ4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -620,6 +637,7 @@ static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   a.Hkv = L.Hkv;
   a.Sq = L.Sq;
   a.Sk = L.Sk;
+  a.Scap = L.Scap;
   a.q_pos_offset = L.q_pos_offset;
   a.causal = L.causal;
   a.n_qtiles = (L.Sq + kBM - 1) / kBM;
@@ -630,13 +648,18 @@ static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int D, bool BF16>
+static cudaError_t launch_fmt(const PrefillLaunch& L, cudaStream_t stream) {
+  if (L.kq4) return L.vq4 ? launch_t<D, BF16, true, true>(L, stream)
+                          : launch_t<D, BF16, true, false>(L, stream);
+  return L.vq4 ? launch_t<D, BF16, false, true>(L, stream)
+               : launch_t<D, BF16, false, false>(L, stream);
+}
+
 cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream) {
-  if (L.D == 128) {
-    if (L.q4) return L.bf16 ? launch_t<128, true, true>(L, stream) : launch_t<128, false, true>(L, stream);
-    return L.bf16 ? launch_t<128, true, false>(L, stream) : launch_t<128, false, false>(L, stream);
-  }
-  if (L.q4) return L.bf16 ? launch_t<64, true, true>(L, stream) : launch_t<64, false, true>(L, stream);
-  return L.bf16 ? launch_t<64, true, false>(L, stream) : launch_t<64, false, false>(L, stream);
+  if (L.D == 128)
+    return L.bf16 ? launch_fmt<128, true>(L, stream) : launch_fmt<128, false>(L, stream);
+  return L.bf16 ? launch_fmt<64, true>(L, stream) : launch_fmt<64, false>(L, stream);
 }
 
 uint32_t prefill_take_error() {

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     assert fa.fa_status_string(0) == "FA_OK"
     assert fa.fa_status_string(4) == "FA_ERR_TIMEOUT"
-    assert fa.fa_version() == 100
+    assert fa.fa_version() == 101
 
 
 def test_q4_0_sizes(lib):
@@ -105,3 +105,26 @@ def test_quantize_bad_arguments(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         fa.load_from(str(tmp_path / "missing.so"))
+
+
+@pytest.mark.parametrize("args,expect", [
+    # q, k, v, o, B, Hq, Hkv, Sq, Sk, cap, D, off, causal, scale, dtype, kf, vf
+    ((P, P, P, P, 1, 8, 2, 4, 64, 32, 64, 60, 1, 0.125, 0, 0, 1), fa.FA_ERR_INVALID_ARG),  # cap < Sk
+    ((P, P, P, P, 1, 8, 2, 4, 64, 64, 64, 60, 1, 0.125, 0, 0, 7), fa.FA_ERR_INVALID_ARG),  # v fmt
+    ((P, P, P, P, 1, 8, 2, 4, 64, 64, 64, 60, 1, 0.125, 0, 3, 1), fa.FA_ERR_INVALID_ARG),  # k fmt
+    ((P, P, P, P, 1, 8, 2, 4, 64, 64, 96, 60, 1, 0.125, 0, 1, 0), fa.FA_ERR_UNSUPPORTED),  # D
+])
+def test_fwd_kv_bad_arguments_rejected_on_host(lib, args, expect):
+    assert lib.fa_fwd_kv(*args, None, 0, None, None) == expect
+
+
+@pytest.mark.parametrize("args", [
+    # k_new, v_new, k_cache, v_cache, B, H, S_new, capacity, pos0, D, dtype
+    (P, P, P, P, 1, 2, 16, 64, 49, 128, 0),   # pos0 + S_new > capacity
+    (P, P, P, P, 1, 2, 16, 64, -1, 128, 0),   # pos0 < 0
+    (P, P, P, P, 1, 2, 16, 64, 0, 48, 0),     # D % 32
+    (P, 0, P, P, 1, 2, 16, 64, 0, 128, 0),    # v_new without v_cache
+    (P, P, P, P, 1, 2, 16, 64, 0, 128, 2),    # dtype
+])
+def test_append_bad_arguments_rejected_on_host(lib, args):
+    assert lib.fa_append_q4_0(*args, None) == fa.FA_ERR_INVALID_ARG
