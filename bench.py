@@ -406,6 +406,41 @@ def other_legs(fa, dev, stream, flush, peaks):
         "frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
         "kv_bytes_per_call": nbytes}
     del q, k, vq, o
+    # paged q4_0 decode: the 4 x 65536-key workload through 256-token pages in shuffled order,
+    # and a batch of four different lengths
+    w = fa_inputs.WORKLOADS[DECODE_WORKLOAD]
+    page = 256
+    for name, lens in (("decode_paged_q4_0_b4_gqa32x8_d128_page256_65536x4", [65536] * 4),
+                       ("decode_paged_q4_0_varlen_gqa32x8_d128_page256_65536_32768_16384_8192",
+                        [65536, 32768, 16384, 8192])):
+        B = len(lens)
+        npages = [n // page for n in lens]
+        NP = sum(npages)
+        g = torch.Generator(device=dev).manual_seed(1006)
+        perm = torch.randperm(NP, generator=g, device=dev).to(torch.int32)
+        table = torch.zeros(B, max(npages), dtype=torch.int32, device=dev)
+        at = 0
+        for b, n in enumerate(npages):
+            table[b, :n] = perm[at:at + n]
+            at += n
+        pool = torch.randn(NP, w.Hkv, page, w.D, generator=g, device=dev).to(torch.float16)
+        kp = fa.fa_quantize_q4_0(pool)
+        pool.normal_(generator=g)
+        vp = fa.fa_quantize_q4_0(pool)
+        del pool
+        q = torch.randn(B, w.Hq, 1, w.D, generator=g, device=dev).to(torch.float16)
+        o = torch.empty_like(q)
+        sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+        ws = torch.empty(fa.load().fa_decode_paged_workspace_bytes(B, w.Hq, w.Hkv, w.D, page,
+                                                                  table.shape[1]),
+                         dtype=torch.uint8, device=dev)
+        ms = time_calls(lambda: fa.fa_decode_paged(q, kp, vp, table, sl, o, workspace=ws), 100, 5,
+                        stream=stream)
+        nbytes = 2 * w.Hkv * sum(lens) * (w.D // 2 + w.D // 16)
+        out[name] = {"us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                     "kv_bytes_per_call": nbytes}
+        del kp, vp, q, o, table, sl, ws
     # append a 16K-token chunk of K and V (B 4, 8 kv heads) into q4_0 caches of 64K tokens
     w = fa_inputs.WORKLOADS[DECODE_WORKLOAD]
     kn = torch.randn(w.B, w.Hkv, 16384, w.D, device=dev).to(torch.float16)

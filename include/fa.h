@@ -145,6 +145,33 @@ fa_status fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, voi
                                 float scale, fa_dtype dtype, fa_kv_format kv_format,
                                 fa_stream_t stream);
 
+/* Decode for a batch of sequences of different lengths over a paged K/V cache: the batch-4
+ * server session named in "perf(rocm): defer SDPA accumulator rescale, stage Q once per block
+ * (#2306)", Conversation (benchmark session page), with the cache of "FlashAttention on gfx90a:
+ * Why It's Broken and How to Fix It", Impact of the V Dequant Patch, kept in q4_0.
+ *  q, o        : [B, Hq, 1, D] in `dtype`; sequence b's query is its last token and sees all of
+ *                its seq_lens[b] keys
+ *  k_pages,
+ *  v_pages     : page pools [num_pages, Hkv, page_size, D], each dense (dtype of Q) or a q4_0
+ *                tensor built for that shape (fa_q4_0_bytes(num_pages, Hkv, page_size, D))
+ *  block_table : device int32 [B, pages_per_seq]: physical page of logical page p of sequence b
+ *                (entries past a sequence's last page are not read)
+ *  seq_lens    : device int32 [B], 1 <= seq_lens[b] <= pages_per_seq * page_size
+ *  page_size   : a multiple of 128 tokens when either side is q4_0, of 64 otherwise
+ *  workspace   : >= fa_decode_paged_workspace_bytes(...) bytes, contents on entry irrelevant
+ *                (see fa_fwd_ex); the split plan is sized for the longest possible sequence.
+ * Host-side checks return FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED; a page number or length out of
+ * range found on the device is recorded (that tile reads zeros) and fa_get_status then returns
+ * FA_ERR_INVALID_ARG. */
+size_t fa_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size,
+                                       int pages_per_seq);
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o,
+                          const int32_t* block_table, const int32_t* seq_lens, int B, int Hq,
+                          int Hkv, int D, int num_pages, int page_size, int pages_per_seq,
+                          float scale, fa_dtype dtype, fa_kv_format k_format,
+                          fa_kv_format v_format, void* workspace, size_t workspace_bytes,
+                          fa_stream_t stream);
+
 /* Size in bytes of a q4_0 tensor for a [B, H, S, D] source, and the offset of its scale plane. */
 size_t fa_q4_0_bytes(int B, int H, int S, int D);
 size_t fa_q4_0_scale_offset(int B, int H, int S, int D);
@@ -171,8 +198,9 @@ fa_status fa_append_q4_0(const void* k_new, const void* v_new, void* k_cache, vo
 
 /* Synchronize `stream`, then report (and clear) any device-side error recorded by this
  * library's kernels since the last call: FA_ERR_TIMEOUT when a bounded wait inside a kernel ran
- * out (the kernel then abandoned its work and returned), FA_ERR_CUDA when the stream reports a
- * CUDA error, FA_OK otherwise. */
+ * out (the kernel then abandoned its work and returned), FA_ERR_INVALID_ARG when a device-side
+ * index input was out of range (fa_decode_paged), FA_ERR_CUDA when the stream reports a CUDA
+ * error, FA_OK otherwise. */
 fa_status fa_get_status(fa_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */
@@ -184,7 +212,8 @@ const char* fa_status_string(fa_status s);
  * or hang is involved. */
 fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream);
 
-/* Library ABI version (major * 100 + minor): 101 adds fa_fwd_kv and fa_append_q4_0. */
+/* Library ABI version (major * 100 + minor): 101 adds fa_fwd_kv and fa_append_q4_0, 102
+ * fa_decode_paged. */
 int fa_version(void);
 
 #ifdef __cplusplus

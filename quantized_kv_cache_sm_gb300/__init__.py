@@ -25,7 +25,8 @@ FA_KV_DENSE, FA_KV_Q4_0 = 0, 1
 EXPORTED = (
     "fa_fwd", "fa_fwd_ex", "fa_workspace_bytes", "fa_q4_0_bytes", "fa_q4_0_scale_offset",
     "fa_quantize_q4_0", "fa_get_status", "fa_status_string", "fa_debug_wait_timeout",
-    "fa_version", "fa_fwd_decode_noalloc", "fa_fwd_kv", "fa_append_q4_0",
+    "fa_version", "fa_fwd_decode_noalloc", "fa_fwd_kv", "fa_append_q4_0", "fa_decode_paged",
+    "fa_decode_paged_workspace_bytes",
 )
 
 _lib = None
@@ -84,6 +85,11 @@ def load_from(p: str) -> ctypes.CDLL:
     lib.fa_fwd_kv.restype = i
     lib.fa_append_q4_0.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.fa_append_q4_0.restype = i
+    lib.fa_decode_paged_workspace_bytes.argtypes = [i] * 6
+    lib.fa_decode_paged_workspace_bytes.restype = sz
+    lib.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp,
+                                    sz, vp]
+    lib.fa_decode_paged.restype = i
     return lib
 
 
@@ -351,3 +357,43 @@ def fa_append_q4_0(k_new: torch.Tensor, k_cache: Q4Tensor, pos0: int,
                                  v_cache.data_ptr() if v_cache is not None else None, B, H, S_new,
                                  k_cache.S, int(pos0), D, _dtype_code(k_new.dtype),
                                  _stream(stream)), "fa_append_q4_0")
+
+
+def fa_decode_paged(q, k_pages, v_pages, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                    o=None, *, scale: float | None = None,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode one token per sequence over paged K/V pools.  q [B, Hq, 1, D]; k_pages, v_pages
+    [num_pages, Hkv, page_size, D] each dense (dtype of q) or a Q4Tensor of that shape;
+    block_table int32 [B, pages_per_seq] and seq_lens int32 [B] on the device."""
+    if o is None:
+        o = torch.empty_like(q)
+    if q.dim() != 4 or q.shape[2] != 1 or not q.is_contiguous() or o.shape != q.shape:
+        raise ValueError("q and o must be contiguous [B, Hq, 1, D] tensors")
+    kf, (NP, Hkv, page, Dk) = _side(k_pages)
+    vf, vshape = _side(v_pages)
+    if vshape != (NP, Hkv, page, Dk):
+        raise ValueError("k_pages and v_pages must have the same [num_pages, Hkv, page_size, D]")
+    B, Hq, _, D = q.shape
+    if Dk != D:
+        raise ValueError("head dim of the pools does not match q")
+    for t, f in ((k_pages, kf), (v_pages, vf)):
+        if f == FA_KV_DENSE and t.dtype != q.dtype:
+            raise TypeError("dense pools must have the dtype of q")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+            or not block_table.is_contiguous():
+        raise ValueError("block_table must be a contiguous int32 [B, pages_per_seq] tensor")
+    if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,):
+        raise ValueError("seq_lens must be an int32 [B] tensor")
+    pps = block_table.shape[1]
+    lib = load()
+    if workspace is None:
+        need = lib.fa_decode_paged_workspace_bytes(B, Hq, Hkv, D, page, pps)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if scale is None:
+        scale = D ** -0.5
+    _check(lib.fa_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(),
+                               block_table.data_ptr(), seq_lens.data_ptr(), B, Hq, Hkv, D, NP,
+                               page, pps, float(scale), _dtype_code(q.dtype), kf, vf,
+                               workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "fa_decode_paged")
+    return o

@@ -297,6 +297,97 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
                    kv_format, kv_format, workspace, workspace_bytes, rescale_count, stream);
 }
 
+// paged decode scratch: flags [Hkv, NT] u32 (256-B padded) then partials [Hkv, NT, G, D + 4]
+// f32, NT = CTAs per kv head
+static size_t paged_workspace(int B, int Hq, int Hkv, int D, bool kq4, bool vq4, int* nt_out) {
+  const int nt = decode_paged_ctas(B, Hkv, num_sms(), kq4, vq4);
+  if (nt_out) *nt_out = nt;
+  return decode_flag_bytes(1, Hkv, nt) + static_cast<size_t>(Hq) * nt * (D + 4) * sizeof(float);
+}
+
+size_t fa_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int D, int page_size,
+                                       int pages_per_seq) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || page_size < 1 || pages_per_seq < 1) return 0;
+  if (D != 64 && D != 128) return 0;
+  size_t m = 0;
+  for (int f = 0; f < 3; ++f) {  // both q4_0, both dense, one of each
+    const size_t w = paged_workspace(B, Hq, Hkv, D, f != 1, f == 0, nullptr);
+    if (w > m) m = w;
+  }
+  return m;
+}
+
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o,
+                          const int32_t* block_table, const int32_t* seq_lens, int B, int Hq,
+                          int Hkv, int D, int num_pages, int page_size, int pages_per_seq,
+                          float scale, fa_dtype dtype, fa_kv_format k_format,
+                          fa_kv_format v_format, void* workspace, size_t workspace_bytes,
+                          fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o))
+    return FA_ERR_INVALID_ARG;
+  if (!block_table || !seq_lens || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return FA_ERR_INVALID_ARG;
+  if (num_pages < 1 || page_size < 1 || pages_per_seq < 1) return FA_ERR_INVALID_ARG;
+  const int64_t max_len = static_cast<int64_t>(page_size) * pages_per_seq;
+  if (max_len > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  // the shape checks of a decode over max_len keys (the longest sequence the table can hold)
+  fa_status st = check_common(B, Hq, Hkv, 1, static_cast<int>(max_len), D,
+                              static_cast<int>(max_len) - 1, 1, scale, dtype, k_format);
+  if (st != FA_OK) return st;
+  if (v_format != FA_KV_DENSE && v_format != FA_KV_Q4_0) return FA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_pages) * Hkv * page_size * D >= (1LL << 40))
+    return FA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_pages) * Hkv >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  const bool bf16 = dtype == FA_BF16;
+  const bool kq4 = k_format == FA_KV_Q4_0;
+  const bool vq4 = v_format == FA_KV_Q4_0;
+  const uint32_t tile = static_cast<uint32_t>(decode_tile_keys(kq4, vq4));
+  if (page_size % static_cast<int>(tile) != 0) return FA_ERR_UNSUPPORTED;
+  int nt = 1;
+  const size_t need = paged_workspace(B, Hq, Hkv, D, kq4, vq4, &nt);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return FA_ERR_INVALID_ARG;
+  const CUtensorMapDataType tdt =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle nib_sw =
+      D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  const uint64_t rows = static_cast<uint64_t>(num_pages) * Hkv;  // (page, kv head) blocks
+  const size_t scale_off = q4_scale_offset(static_cast<int64_t>(rows) * page_size, D);
+  DecodeLaunch L;
+  if (!kv_map(&L.tm_k, k_pages, kq4, tdt, D, page_size, rows, tile, nib_sw) ||
+      !kv_map(&L.tm_v, v_pages, vq4, tdt, D, page_size, rows, tile, nib_sw))
+    return FA_ERR_CUDA;
+  L.k_scale = kq4 ? static_cast<const uint8_t*>(k_pages) + scale_off : nullptr;
+  L.v_scale = vq4 ? static_cast<const uint8_t*>(v_pages) + scale_off : nullptr;
+  L.q = q;
+  L.o = o;
+  L.flags = static_cast<uint32_t*>(workspace);
+  L.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                       decode_flag_bytes(1, Hkv, nt));
+  L.tag = next_call_tag();
+  L.B = B;
+  L.Hq = Hq;
+  L.Hkv = Hkv;
+  L.Sk = static_cast<int>(max_len);
+  L.Scap = page_size;
+  L.Sk_eff = static_cast<int>(max_len);
+  L.D = D;
+  L.nsplit = nt;
+  L.chunk = 0;
+  L.scale = scale;
+  L.bf16 = bf16;
+  L.kq4 = kq4;
+  L.vq4 = vq4;
+  L.block_table = block_table;
+  L.seq_lens = seq_lens;
+  L.page_size = page_size;
+  L.pages_per_seq = pages_per_seq;
+  L.num_pages = num_pages;
+  return decode_launch(L, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                 : FA_ERR_CUDA;
+}
+
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
                  int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
                  fa_dtype dtype, fa_kv_format kv_format, fa_stream_t stream) {
@@ -327,6 +418,7 @@ fa_status fa_get_status(fa_stream_t stream) {
   if (c != 0 && cudaMemcpyToSymbol(g_debug_error, &z, sizeof(z)) != cudaSuccess)
     return FA_ERR_CUDA;
   if (a == 0xffffffffu || b == 0xffffffffu) return FA_ERR_CUDA;
+  if (b == kErrBadIndex) return FA_ERR_INVALID_ARG;
   if (a || b || c) return FA_ERR_TIMEOUT;
   return FA_OK;
 }
@@ -350,6 +442,6 @@ fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream) {
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_version(void) { return 101; }
+int fa_version(void) { return 102; }
 
 }  // extern "C"

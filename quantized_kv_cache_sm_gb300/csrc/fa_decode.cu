@@ -192,9 +192,15 @@ struct DecodeArgs {
   uint32_t tag;
   int Hq, Hkv, Sk, Sk_eff, nsplit, chunk;
   float scale_log2;
+  // paged cache (PAGED kernels): K/V pages [num_pages][Hkv][page_size][D], logical page p of
+  // sequence b at block_table[b * pages_per_seq + p], seq_lens[b] tokens in sequence b
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int page_size, pages_per_seq, num_pages;
+  int B;
 };
 
-template <int D, bool BF16, bool KQ4, bool VQ4>
+template <int D, bool BF16, bool KQ4, bool VQ4, bool PAGED>
 __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs args) {
@@ -212,12 +218,61 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
   const int hkv = blockIdx.y;
-  const int b = blockIdx.z;
   const int G = args.Hq / args.Hkv;
-  const int kb0 = split * args.chunk;
-  const int kb1 = min(args.Sk_eff, kb0 + args.chunk);
+  // (sequence, split) of this CTA, this sequence's visible keys, split length and split count.
+  // Uniform batch: grid (split, kv head, batch).  Paged batch: grid (CTA, kv head); the CTAs of
+  // a kv head are shared out over the sequences in proportion to their lengths (in tiles), every
+  // CTA computing the same plan from seq_lens; CTAs past the plan have nothing to do.
+  int b = blockIdx.z, split = blockIdx.x;
+  int sk_b = args.Sk_eff, chunk = args.chunk, nsplit_b = args.nsplit;
+  int first = 0;  // paged: the plan index of this sequence's first CTA
+  if constexpr (PAGED) {
+    const int cap = args.pages_per_seq * args.page_size;
+    auto len_of = [&](int bb) {
+      const int n = args.seq_lens[bb];
+      return max(1, min(n, cap));
+    };
+    int64_t total = 0;  // tiles of the whole batch
+    for (int bb = 0; bb < args.B; ++bb) total += (len_of(bb) + kTileKeys - 1) / kTileKeys;
+    const int spare = args.nsplit - args.B;  // CTAs beyond one per sequence
+    int s = blockIdx.x;
+    b = -1;
+    for (int bb = 0; bb < args.B; ++bb) {
+      const int t = (len_of(bb) + kTileKeys - 1) / kTileKeys;
+      const int ns = 1 + static_cast<int>(static_cast<int64_t>(spare) * t / total);
+      if (s < ns) {
+        b = bb;
+        split = s;
+        nsplit_b = ns;
+        first = static_cast<int>(blockIdx.x) - s;
+        break;
+      }
+      s -= ns;
+    }
+    if (b < 0) return;  // nothing planned for this CTA (no barrier or memory touched yet)
+    sk_b = args.seq_lens[b];
+    if (sk_b < 1 || sk_b > cap) {
+      if (threadIdx.x == 0 && split == 0 && hkv == 0)
+        atomicCAS(&g_decode_error, kErrNone, kErrBadIndex);
+      sk_b = max(1, min(sk_b, cap));
+    }
+    const int tiles = (sk_b + kTileKeys - 1) / kTileKeys;
+    chunk = (tiles + nsplit_b - 1) / nsplit_b * kTileKeys;
+  }
+  // slots of the partials and flags.  Uniform batch: [B, Hq, nsplit] partial rows, [B, Hkv,
+  // nsplit] flags.  Paged batch: one slot per (kv head, plan CTA): [Hkv, nsplit, G] partial rows,
+  // [Hkv, nsplit] flags, a sequence's slots being consecutive -- independent of the batch size.
+  const int64_t row0 = static_cast<int64_t>(b) * args.Hq + static_cast<int64_t>(hkv) * G;
+  const int64_t part_base = PAGED ? (static_cast<int64_t>(hkv) * args.nsplit + first) * G
+                                  : row0 * args.nsplit;
+  const int64_t head_stride = PAGED ? 1 : args.nsplit;
+  const int64_t slot_stride = PAGED ? G : 1;
+  const int64_t flag_base = PAGED ? static_cast<int64_t>(hkv) * args.nsplit + first
+                                  : (static_cast<int64_t>(b) * args.Hkv + hkv) * args.nsplit;
+  const int sk_lim = PAGED ? sk_b : args.Sk;  // keys stored (scale rows past it are not read)
+  const int kb0 = split * chunk;
+  const int kb1 = min(sk_b, kb0 + chunk);
   const int ntiles = (kb1 - kb0 + kTileKeys - 1) / kTileKeys;
   const int64_t bh = static_cast<int64_t>(b) * args.Hkv + hkv;
 
@@ -243,6 +298,22 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
     for (; n < ntiles; ++n) {
       const int s = n % C::kStages;
       const int key0 = kb0 + n * kTileKeys;
+      // where the tile lives: row tma_row of (page or (batch, kv head)) block tma_bh; a tile
+      // never straddles pages (page_size is a multiple of the tile)
+      int tma_row = key0;
+      int64_t tma_bh = bh;
+      int64_t rows_per_bh = args.Scap;
+      if constexpr (PAGED) {
+        const int lp = key0 / args.page_size;
+        int page = args.block_table[static_cast<int64_t>(b) * args.pages_per_seq + lp];
+        if (page < 0 || page >= args.num_pages) {
+          if (lane == 0) atomicCAS(&g_decode_error, kErrNone, kErrBadIndex);
+          page = -1;  // TMA rows out of the map read as zeros; scale loads are skipped
+        }
+        tma_row = key0 - lp * args.page_size;
+        tma_bh = static_cast<int64_t>(page) * args.Hkv + hkv;
+        rows_per_bh = args.page_size;
+      }
       // q4_0: this lane's scale rows (keys 4*lane .. 4*lane+3 of the tile), zero past Sk; the
       // loads are issued before waiting for the slot so their latency overlaps the wait
       uint32_t kr[kKeysPerLane][2], vr[kKeysPerLane][2];
@@ -251,8 +322,8 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
         for (int j = 0; j < kKeysPerLane; ++j) {
           const int key = key0 + kKeysPerLane * lane + j;
           kr[j][0] = kr[j][1] = vr[j][0] = vr[j][1] = 0u;
-          if (key < args.Sk) {
-            const int64_t off = (bh * args.Scap + key) * C::kRow;
+          if (key < sk_lim && tma_bh >= 0) {
+            const int64_t off = (tma_bh * rows_per_bh + (tma_row + (key - key0))) * C::kRow;
             if (kNB == 4) {
               if (KQ4) {
                 const uint2 a = __ldg(reinterpret_cast<const uint2*>(args.k_scale + off));
@@ -280,20 +351,20 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_full + 8 * s, C::kKBytes + C::kVBytes);
         if constexpr (KQ4) {
-          tma_load_3d(st, &tm_k, bar_full + 8 * s, 0, key0, static_cast<int>(bh));
+          tma_load_3d(st, &tm_k, bar_full + 8 * s, 0, tma_row, static_cast<int>(tma_bh));
         } else {
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(st + c * (kTileKeys * 128), &tm_k, bar_full + 8 * s, 64 * c, key0,
-                        static_cast<int>(bh));
+            tma_load_3d(st + c * (kTileKeys * 128), &tm_k, bar_full + 8 * s, 64 * c, tma_row,
+                        static_cast<int>(tma_bh));
         }
         if constexpr (VQ4) {
-          tma_load_3d(st + C::kOffV, &tm_v, bar_full + 8 * s, 0, key0, static_cast<int>(bh));
+          tma_load_3d(st + C::kOffV, &tm_v, bar_full + 8 * s, 0, tma_row, static_cast<int>(tma_bh));
         } else {
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(st + C::kOffV + c * (kTileKeys * 128), &tm_v, bar_full + 8 * s, 64 * c,
-                        key0, static_cast<int>(bh));
+                        tma_row, static_cast<int>(tma_bh));
         }
       }
       if constexpr (Q4) {
@@ -691,7 +762,6 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
   }
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
   const int tid = threadIdx.x - 32;  // 0..127
-  const int64_t row0 = static_cast<int64_t>(b) * args.Hq + static_cast<int64_t>(hkv) * G;
   for (int idx = tid; idx < G * (D + 2); idx += 32 * kConsumers) {
     const int hh = idx / (D + 2);
     const int c = idx % (D + 2);
@@ -711,7 +781,8 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
       }
       out = acc;
     }
-    float* dst = args.partial + ((row0 + hh) * args.nsplit + split) * C::kPartStride;
+    float* dst =
+        args.partial + (part_base + hh * head_stride + split * slot_stride) * C::kPartStride;
     dst[c == 0 ? 0 : (c == 1 ? 1 : c + 2)] = out;
   }
 
@@ -726,13 +797,13 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
   volatile uint32_t* is_last =
       reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 16 * C::kStages + 8);
-  uint32_t* flags = args.flags + bh * args.nsplit;
+  uint32_t* flags = args.flags + flag_base;
   if (cw == 0) {
     if (lane == 0) st_release_gpu(flags + split, args.tag);
     __syncwarp();
     fence_sc_gpu();  // the whole warp: its flag loads below come after the store above
     bool all = true;
-    for (int s = lane; s < args.nsplit; s += 32) all = all && ld_relaxed_gpu(flags + s) == args.tag;
+    for (int s = lane; s < nsplit_b; s += 32) all = all && ld_relaxed_gpu(flags + s) == args.tag;
     all = __all_sync(0xffffffffu, all);
     if (all) fence_acq_rel_gpu();  // the partials behind the flags are read after this
     if (lane == 0) *is_last = all ? 1u : 0u;
@@ -740,38 +811,39 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers) : "memory");
   if (*is_last == 0u) return;
   if (cw == 0)
-    for (int s = lane; s < args.nsplit; s += 32) st_relaxed_gpu(flags + s, 0u);
+    for (int s = lane; s < nsplit_b; s += 32) st_relaxed_gpu(flags + s, 0u);
   constexpr int kPer = D / 32;  // head-dim elements per lane
   constexpr int kStride = C::kPartStride;
   for (int hh = cw; hh < G; hh += kConsumers) {
-    const float* p = args.partial + (row0 + hh) * args.nsplit * kStride;
+    const float* p = args.partial + (part_base + hh * head_stride) * kStride;
+    const int64_t ss = slot_stride * kStride;  // floats from one split's row to the next
     // (m_s, l_s) with the splits across the lanes, 32 at a time; the first 32 stay in registers
     float2 ml0 = make_float2(-INFINITY, 0.f);
-    if (lane < args.nsplit) ml0 = __ldcg(reinterpret_cast<const float2*>(p + lane * kStride));
+    if (lane < nsplit_b) ml0 = __ldcg(reinterpret_cast<const float2*>(p + lane * ss));
     float M = ml0.x;
-    for (int s = lane + 32; s < args.nsplit; s += 32) M = fmaxf(M, __ldcg(p + s * kStride));
+    for (int s = lane + 32; s < nsplit_b; s += 32) M = fmaxf(M, __ldcg(p + s * ss));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    for (int s0 = 0; s0 < args.nsplit; s0 += 32) {
+    for (int s0 = 0; s0 < nsplit_b; s0 += 32) {
       float2 ml = ml0;
       if (s0 > 0) {
         ml = make_float2(-INFINITY, 0.f);
-        if (s0 + lane < args.nsplit)
-          ml = __ldcg(reinterpret_cast<const float2*>(p + (s0 + lane) * kStride));
+        if (s0 + lane < nsplit_b)
+          ml = __ldcg(reinterpret_cast<const float2*>(p + (s0 + lane) * ss));
       }
       const float wl = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - M);  // e^(m_s - M), lane s
       L = fmaf(wl, ml.y, L);
-      const int n = min(32, args.nsplit - s0);
+      const int n = min(32, nsplit_b - s0);
       // O_s rows, eight splits' loads in flight before their multiply-adds (in split order)
       for (int j0 = 0; j0 < n; j0 += 8) {
         float x[8][kPer];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float* row = p + (s0 + j0 + j) * kStride + 4;
+          const float* row = p + (s0 + j0 + j) * ss + 4;
           if (j0 + j < n) {
             if constexpr (kPer == 4) {
               const float4 v = __ldcg(reinterpret_cast<const float4*>(row) + lane);
@@ -827,6 +899,13 @@ static int decode_ctas_per_sm(bool kq4, bool vq4) {
   return DCfg<128, false, false>::kCtasPerSm;
 }
 
+int decode_paged_ctas(int B, int Hkv, int num_sms, bool kq4, bool vq4) {
+  // one wave of CTAs at the kernel's resident count, at least one per sequence
+  const int slots = (num_sms < 1 ? 1 : num_sms) * decode_ctas_per_sm(kq4, vq4);
+  const int per_head = slots / (Hkv < 1 ? 1 : Hkv);
+  return per_head > B ? per_head : B;
+}
+
 void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool kq4, bool vq4, int* nsplit,
                  int* chunk) {
   // one wave of CTAs at the kernel's resident count, equal key chunks of whole tiles
@@ -848,7 +927,8 @@ void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool kq4, bool vq4, in
 template <int D, bool BF16, bool KQ4, bool VQ4>
 static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   using C = DCfg<D, KQ4, VQ4>;
-  auto kern = decode_split_kernel<D, BF16, KQ4, VQ4>;
+  auto kern = L.block_table ? decode_split_kernel<D, BF16, KQ4, VQ4, true>
+                            : decode_split_kernel<D, BF16, KQ4, VQ4, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -859,6 +939,12 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   a.o = static_cast<uint16_t*>(L.o);
   a.partial = L.partial;
   a.Scap = L.Scap;
+  a.block_table = L.block_table;
+  a.seq_lens = L.seq_lens;
+  a.page_size = L.page_size;
+  a.pages_per_seq = L.pages_per_seq;
+  a.num_pages = L.num_pages;
+  a.B = L.B;
   a.flags = L.flags;
   a.tag = L.tag;
   a.Hq = L.Hq;
@@ -868,7 +954,8 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   a.nsplit = L.nsplit;
   a.chunk = L.chunk;
   a.scale_log2 = L.scale * kLog2e;
-  dim3 grid(L.nsplit, L.Hkv, L.B);
+  // paged: nsplit CTAs per kv head shared over the batch (the plan is made on the device)
+  const dim3 grid = L.block_table ? dim3(L.nsplit, L.Hkv, 1) : dim3(L.nsplit, L.Hkv, L.B);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, a);
   return cudaGetLastError();
 }

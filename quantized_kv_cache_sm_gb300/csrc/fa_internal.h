@@ -32,6 +32,11 @@ struct DecodeLaunch {
   int B, Hq, Hkv, Sk_eff, Sk, Scap, D, nsplit, chunk;
   float scale;
   bool bf16, kq4, vq4;
+  // paged cache (block_table != nullptr): pages [num_pages][Hkv][page_size][D]; per-sequence
+  // lengths on the device; Sk_eff then bounds every sequence's length
+  const int32_t* block_table = nullptr;
+  const int32_t* seq_lens = nullptr;
+  int page_size = 0, pages_per_seq = 0, num_pages = 0;
 };
 cudaError_t decode_launch(const DecodeLaunch& L, cudaStream_t stream);
 uint32_t decode_take_error();
@@ -42,6 +47,8 @@ size_t decode_flag_bytes(int B, int Hkv, int nsplit);
 void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool kq4, bool vq4, int* nsplit,
                  int* chunk);
 int decode_tile_keys(bool kq4, bool vq4);
+// CTAs per kv head of a paged decode launch (shared over the batch on the device)
+int decode_paged_ctas(int B, int Hkv, int num_sms, bool kq4, bool vq4);
 
 // q4_0 quantization of up to two tensors in one launch (job 1 may be absent: x1 == nullptr).
 // Source rows [B*H][S_src][D]; row (bh, s) goes to destination row bh * Scap + pos0 + s.

@@ -16,6 +16,7 @@ namespace fa {
 enum : uint32_t {
   kErrNone = 0,
   kErrTimeout = 1,  // a bounded wait ran out
+  kErrBadIndex = 2,  // a device-side index input (page number, sequence length) was out of range
 };
 
 // A wait that has not completed after this long is treated as a hang (the longest legitimate

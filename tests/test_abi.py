@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     assert fa.fa_status_string(0) == "FA_OK"
     assert fa.fa_status_string(4) == "FA_ERR_TIMEOUT"
-    assert fa.fa_version() == 101
+    assert fa.fa_version() == 102
 
 
 def test_q4_0_sizes(lib):
@@ -128,3 +128,19 @@ def test_fwd_kv_bad_arguments_rejected_on_host(lib, args, expect):
 ])
 def test_append_bad_arguments_rejected_on_host(lib, args):
     assert lib.fa_append_q4_0(*args, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_paged_decode_host_checks(lib):
+    T = P + 256  # a 4-byte aligned fake table / length pointer
+    base = [P, P, P, P, T, T, 2, 8, 2, 128, 16, 128, 8, 0.088, 0, 1, 1, P, 1 << 30, None]
+    # every case below is rejected by the host checks, before any tensor map or launch
+    bad_page = list(base)
+    bad_page[11] = 96  # page_size not a multiple of the 128-key q4_0 tile
+    assert lib.fa_decode_paged(*bad_page) in (fa.FA_ERR_UNSUPPORTED,)
+    no_table = list(base)
+    no_table[4] = None
+    assert lib.fa_decode_paged(*no_table) == fa.FA_ERR_INVALID_ARG
+    big_group = list(base)
+    big_group[7], big_group[8] = 32, 2  # 16 query heads per kv head
+    assert lib.fa_decode_paged(*big_group) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_decode_paged_workspace_bytes(2, 8, 3, 128, 128, 8) == 0  # Hq % Hkv
