@@ -406,6 +406,21 @@ def other_legs(fa, dev, stream, flush, peaks):
         "frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
         "kv_bytes_per_call": nbytes}
     del q, k, vq, o
+    # the explicit (non-flash) path on the q4_0 16K chunk: dequant, S in f32, softmax, O = P V
+    w = fa_inputs.WORKLOADS["prefill_q4_0_gqa32x8_d128_sq2048_sk16384_f16"]
+    q, k, v = fa_inputs.make_qkv(w, device=dev, generate_on_device=True)
+    kq, vq = fa.fa_quantize_q4_0(k), fa.fa_quantize_q4_0(v)
+    del k, v
+    o = torch.empty_like(q)
+    ws = torch.empty(fa.load().fa_explicit_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, 1, 1),
+                     dtype=torch.uint8, device=dev)
+    ms = time_calls(lambda: fa.fa_fwd_explicit(q, kq, vq, o, causal=True, workspace=ws), 10, 2,
+                    flush=flush, stream=stream)
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    out["explicit_q4_0_gqa32x8_d128_sq2048_sk16384_f16"] = {
+        "ms": round(ms, 4), "TFLOP/s": round(tf, 2), "frac": round(tf / peak, 4),
+        "note": "non-flash path: dequant, S in f32 (batched GEMM), softmax, O = P V (GEMM)"}
+    del q, kq, vq, o, ws
     # paged q4_0 decode: the 4 x 65536-key workload through 256-token pages in shuffled order,
     # and a batch of four different lengths
     w = fa_inputs.WORKLOADS[DECODE_WORKLOAD]

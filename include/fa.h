@@ -172,6 +172,24 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
                           fa_kv_format v_format, void* workspace, size_t workspace_bytes,
                           fa_stream_t stream);
 
+/* The explicit (non-flash) attention path, for comparison with fa_fwd_kv: q4_0 sides are first
+ * expanded to dense f16/bf16, S = scale * Q K^T is written out in f32 by a batched GEMM (cuBLAS),
+ * a softmax kernel makes P (causal mask, rounded to the dtype), and O = P V is a second batched
+ * GEMM.  Approach C of "FlashAttention on gfx90a: Why It's Broken and How to Fix It" (dequantize
+ * K and V, two GEMMs and a softmax), the path that page measures against flash attention.
+ *  Arguments: as fa_fwd_kv without a capacity (K, V: [B, Hkv, Sk, D] each, dense or q4_0).
+ *  workspace: >= fa_explicit_workspace_bytes(...) bytes: S (4 bytes per score), P (2 bytes per
+ *             score) and, per q4_0 side, its dense copy -- B*Hq*Sq*Sk*6 bytes and more, so this
+ *             path is for moderate shapes (Hq = 32, Sq = 2048, Sk = 16384 needs 6.4 GB).
+ *  Errors: as fa_fwd_ex; a failing cuBLAS call gives FA_ERR_CUDA. */
+size_t fa_explicit_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                                   fa_kv_format k_format, fa_kv_format v_format);
+fa_status fa_fwd_explicit(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                          int Hkv, int Sq, int Sk, int D, int q_pos_offset, int causal,
+                          float scale, fa_dtype dtype, fa_kv_format k_format,
+                          fa_kv_format v_format, void* workspace, size_t workspace_bytes,
+                          fa_stream_t stream);
+
 /* Size in bytes of a q4_0 tensor for a [B, H, S, D] source, and the offset of its scale plane. */
 size_t fa_q4_0_bytes(int B, int H, int S, int D);
 size_t fa_q4_0_scale_offset(int B, int H, int S, int D);
@@ -213,7 +231,7 @@ const char* fa_status_string(fa_status s);
 fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream);
 
 /* Library ABI version (major * 100 + minor): 101 adds fa_fwd_kv and fa_append_q4_0, 102
- * fa_decode_paged. */
+ * fa_decode_paged, 103 fa_fwd_explicit. */
 int fa_version(void);
 
 #ifdef __cplusplus

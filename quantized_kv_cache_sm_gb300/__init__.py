@@ -26,7 +26,7 @@ EXPORTED = (
     "fa_fwd", "fa_fwd_ex", "fa_workspace_bytes", "fa_q4_0_bytes", "fa_q4_0_scale_offset",
     "fa_quantize_q4_0", "fa_get_status", "fa_status_string", "fa_debug_wait_timeout",
     "fa_version", "fa_fwd_decode_noalloc", "fa_fwd_kv", "fa_append_q4_0", "fa_decode_paged",
-    "fa_decode_paged_workspace_bytes",
+    "fa_decode_paged_workspace_bytes", "fa_fwd_explicit", "fa_explicit_workspace_bytes",
 )
 
 _lib = None
@@ -90,6 +90,11 @@ def load_from(p: str) -> ctypes.CDLL:
     lib.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp,
                                     sz, vp]
     lib.fa_decode_paged.restype = i
+    lib.fa_explicit_workspace_bytes.argtypes = [i] * 8
+    lib.fa_explicit_workspace_bytes.restype = sz
+    lib.fa_fwd_explicit.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, i, i, vp, sz,
+                                    vp]
+    lib.fa_fwd_explicit.restype = i
     return lib
 
 
@@ -396,4 +401,35 @@ def fa_decode_paged(q, k_pages, v_pages, block_table: torch.Tensor, seq_lens: to
                                page, pps, float(scale), _dtype_code(q.dtype), kf, vf,
                                workspace.data_ptr(), workspace.numel(), _stream(stream)),
            "fa_decode_paged")
+    return o
+
+
+def fa_fwd_explicit(q, k, v, o=None, *, causal: bool = True, q_pos_offset: int | None = None,
+                    scale: float | None = None, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """The explicit (non-flash) path: dense K/V (q4_0 sides expanded first), S = scale Q K^T in
+    f32, softmax, O = P V.  Same arguments as fa_fwd_kv without a capacity."""
+    if o is None:
+        o = torch.empty_like(q)
+    if q.dim() != 4 or not q.is_contiguous() or not o.is_contiguous() or o.shape != q.shape:
+        raise ValueError("q and o must be contiguous [B, Hq, Sq, D] tensors of the same shape")
+    kf, (Bk, Hkv, Sk, Dk) = _side(k)
+    vf, vshape = _side(v)
+    if vshape != (Bk, Hkv, Sk, Dk):
+        raise ValueError("k and v must have the same [B, Hkv, Sk, D]")
+    B, Hq, Sq, D = q.shape
+    if Bk != B or Dk != D:
+        raise ValueError("k/v batch or head dim does not match q")
+    if q_pos_offset is None:
+        q_pos_offset = Sk - Sq
+    if scale is None:
+        scale = D ** -0.5
+    lib = load()
+    if workspace is None:
+        need = lib.fa_explicit_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, kf, vf)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib.fa_fwd_explicit(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv,
+                               Sq, Sk, D, int(q_pos_offset), int(bool(causal)), float(scale),
+                               _dtype_code(q.dtype), kf, vf, workspace.data_ptr(),
+                               workspace.numel(), _stream(stream)), "fa_fwd_explicit")
     return o

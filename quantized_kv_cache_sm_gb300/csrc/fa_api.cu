@@ -388,6 +388,55 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
                                                                                  : FA_ERR_CUDA;
 }
 
+size_t fa_explicit_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                                   fa_kv_format k_format, fa_kv_format v_format) {
+  if (check_common(B, Hq, Hkv, Sq, Sk, D, 0, 0, 1.f, FA_F16, k_format) != FA_OK) return 0;
+  if (v_format != FA_KV_DENSE && v_format != FA_KV_Q4_0) return 0;
+  return explicit_workspace(B, Hq, Hkv, Sq, Sk, D, k_format == FA_KV_Q4_0,
+                            v_format == FA_KV_Q4_0);
+}
+
+fa_status fa_fwd_explicit(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                          int Hkv, int Sq, int Sk, int D, int q_pos_offset, int causal,
+                          float scale, fa_dtype dtype, fa_kv_format k_format,
+                          fa_kv_format v_format, void* workspace, size_t workspace_bytes,
+                          fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  const fa_status st =
+      check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale, dtype, k_format);
+  if (st != FA_OK) return st;
+  if (v_format != FA_KV_DENSE && v_format != FA_KV_Q4_0) return FA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * Hq * Sq > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(Hq / Hkv) * Sq > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const bool kq4 = k_format == FA_KV_Q4_0, vq4 = v_format == FA_KV_Q4_0;
+  const size_t need = explicit_workspace(B, Hq, Hkv, Sq, Sk, D, kq4, vq4);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return FA_ERR_INVALID_ARG;
+  ExplicitLaunch L;
+  L.q = q;
+  L.k = k;
+  L.v = v;
+  L.o = o;
+  L.workspace = workspace;
+  L.scale_offset = q4_scale_offset(static_cast<int64_t>(B) * Hkv * Sk, D);
+  L.B = B;
+  L.Hq = Hq;
+  L.Hkv = Hkv;
+  L.Sq = Sq;
+  L.Sk = Sk;
+  L.D = D;
+  L.q_pos_offset = causal ? q_pos_offset : 0;
+  L.causal = causal ? 1 : 0;
+  L.scale = scale;
+  L.bf16 = dtype == FA_BF16;
+  L.kq4 = kq4;
+  L.vq4 = vq4;
+  int cublas_status = 0;
+  if (explicit_launch(L, reinterpret_cast<cudaStream_t>(stream), &cublas_status) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return cublas_status ? FA_ERR_CUDA : FA_OK;
+}
+
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
                  int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
                  fa_dtype dtype, fa_kv_format kv_format, fa_stream_t stream) {
@@ -442,6 +491,6 @@ fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream) {
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_version(void) { return 102; }
+int fa_version(void) { return 103; }
 
 }  // extern "C"

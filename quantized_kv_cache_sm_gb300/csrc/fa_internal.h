@@ -60,6 +60,23 @@ struct QuantJob {
 cudaError_t quantize_launch(QuantJob j0, QuantJob j1, int64_t BH, int S_src, int Scap, int pos0,
                             int D, bool bf16, cudaStream_t stream);
 
+// the explicit (non-flash) path: dequant (q4_0 sides), S = scale Q K^T (f32), softmax -> P,
+// O = P V; workspace = S, P and the dequantized K / V
+struct ExplicitLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  void* workspace;
+  size_t scale_offset;  // of the q4_0 scale plane within a K or V tensor
+  int B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal;
+  float scale;
+  bool bf16, kq4, vq4;
+};
+size_t explicit_workspace(int B, int Hq, int Hkv, int Sq, int Sk, int D, bool kq4, bool vq4);
+// returns the CUDA launch status; *cublas_status is non-zero when a cuBLAS call failed
+cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* cublas_status);
+
 cudaError_t debug_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
 uint32_t debug_take_error();
 
