@@ -323,13 +323,13 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         }
         // scales: one 4- or 8-byte row per key, zero-filled past Sk
         const uint8_t* sp = is_v ? args.v_scale : args.k_scale;
-        for (int r = lane; r < kBN; r += 32) {
-          const int key = j * kBN + r;
+        for (int row = lane; row < kBN; row += 32) {
+          const int key = j * kBN + row;
           const bool in = key < args.Sk;
           const uint8_t* src =
               sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Scap + (in ? key : 0)) *
                        C::kScaleRow;
-          const uint32_t d = dst + C::kRawNib + r * C::kScaleRow;
+          const uint32_t d = dst + C::kRawNib + row * C::kScaleRow;
           if (C::kScaleRow == 8)
             cp_async_8(d, src, in ? 8u : 0u);
           else
@@ -400,7 +400,8 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         if (j == nb_t - 1) mma_commit(bar(kBarODone + t));
       };
       // order: QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage is
-      // acquired at its first use and released after its last (all in ring order).
+      // acquired at the start of the step that first uses it and released after its last use
+      // (all in ring order).
       if (nbmax > 0 && ok) {
         const int sK = acquire();
         if (ok) {
@@ -410,17 +411,16 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         }
       }
       for (int j = 0; j < nbmax && ok; ++j) {
+        // both ring waits of the step sit next to the P_A wait: an mbarrier wait issued while
+        // the MMA queue is short stalls the issue of the next MMAs, so the waits are grouped
+        // where they cost one stall instead of one per wait
         const int sV = acquire();
+        const bool next = j + 1 < nbmax;
+        const int sK = next ? acquire() : 0;
         if (!ok) break;
         if (j < nbA) issue_pv(0, j, sV, nbA);
         if (!ok) break;
-        const bool next = j + 1 < nbmax;
-        int sK = 0;
-        if (next) {
-          sK = acquire();
-          if (!ok) break;
-          if (j + 1 < nbA) issue_qk(0, sK);
-        }
+        if (next && j + 1 < nbA) issue_qk(0, sK);
         if (j < nbB) issue_pv(1, j, sV, nbB);
         if (!ok) break;
         release(sV);
