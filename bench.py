@@ -206,11 +206,13 @@ def run_ours(args, rank, world, local_rank):
     if w.kv_format == "q4_0":
         k, v = fa.fa_quantize_q4_0(k), fa.fa_quantize_q4_0(v)
     o = torch.empty_like(q)
-    ws = None
     rc = None
-    if w.Sq == 1:
-        ws = torch.empty(fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset,
-                                               w.causal), dtype=torch.uint8, device=dev)
+    # scratch: the decode partials, or the prefill's cut schedule (dense K/V, D = 128) where the
+    # library plans one for this device; without it the prefill runs one work unit per CTA
+    n_ws = fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset, w.causal)
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev) if n_ws > 0 else None
+    kernel = ("prefill_seg_kernel" if w.Sq > 1 and n_ws > 0 and w.kv_format == "dense"
+              and w.D == 128 else "prefill_kernel")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -272,14 +274,14 @@ def run_ours(args, rank, world, local_rank):
             "parallelism": f"replicas x{world} (independent problems per rank)",
         },
         "roofline": {
-            "kernel": "prefill_kernel",
+            "kernel": kernel,
             "bound": "tensor",
             "achieved": round(achieved, 2),
             "peak": peak,
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
             "peak_source": f"{peaks_src} bf16 dense burst (f16 runs at the same rate)",
-            "traffic": measured_traffic(f"prefill_kernel_{w.dtype}_{w.kv_format}", w.name),
+            "traffic": measured_traffic(f"{kernel}_{w.dtype}_{w.kv_format}", w.name),
             "traffic_unit": "bytes per launch (ncu dram read + write)",
             "algorithmic_flops_per_launch": flops,
         },
@@ -318,10 +320,9 @@ def e2e_leg(fa, w, dev, stream, steps, warmup, world):
         bf = {"q": torch.empty_like(q), "k": torch.empty_like(k), "v": torch.empty_like(v),
               "o": torch.empty_like(q), "ho": torch.empty(q.shape, dtype=q.dtype).pin_memory(),
               "ws": None}
-        if w.Sq == 1:
-            bf["ws"] = torch.empty(fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D,
-                                                         w.q_pos_offset, w.causal),
-                                   dtype=torch.uint8, device=dev)
+        n = fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset, w.causal)
+        if n > 0:  # decode partials, or the prefill's cut schedule
+            bf["ws"] = torch.empty(n, dtype=torch.uint8, device=dev)
         bufs.append(bf)
 
     def step(i):

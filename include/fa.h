@@ -71,21 +71,25 @@ typedef enum {
  *  scale     : softmax scale, finite and > 0 (typically 1/sqrt(D))
  * Sq == 1 runs the split-K decode kernels and needs a scratch buffer of fa_workspace_bytes();
  * fa_fwd takes it from the stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on `stream`);
- * use fa_fwd_ex to pass one instead.  Sq >= 2 runs the prefill kernel and needs no scratch. */
+ * use fa_fwd_ex to pass one instead.  Sq >= 2 runs the prefill kernel; where there are more
+ * work units than SMs and cutting them evenly over one CTA per SM is estimated to finish sooner
+ * (dense K/V, D = 128), it uses fa_workspace_bytes() of scratch for the partial rows of units
+ * cut between CTAs; with less scratch (or none) it runs one unit per CTA. */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
                  int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
                  fa_dtype dtype, fa_kv_format kv_format, fa_stream_t stream);
 
 /* fa_fwd with caller-provided scratch and an optional rescale counter.
  *  workspace, workspace_bytes : device buffer of at least fa_workspace_bytes(...) bytes (may be
- *                 NULL when that is 0); owned by the caller, must not be used by another call in
+ *                 NULL when that is 0; for Sq >= 2 a smaller or NULL buffer selects one work
+ *                 unit per CTA); owned by the caller, must not be used by another call in
  *                 flight at the same time.  Its contents on entry do not matter: it holds one
- *                 32-bit arrival flag per split of each (batch, kv head), which the split sets
- *                 to a tag drawn afresh for every call once its partial result is stored, then
- *                 the partial results, which the split that finds all its siblings' flags set
- *                 merges (it also clears those flags).  A call reads only what it wrote itself,
- *                 apart from the flags; a stale flag is mistaken for this call's only if it
- *                 holds exactly the call's 32-bit tag.
+ *                 32-bit arrival flag per split of each (batch, kv head) -- prefill: per piece
+ *                 slot of each CTA -- which is set to a tag drawn afresh for every call once the
+ *                 partial result behind it is stored, then the partial results, which the piece
+ *                 that finds all its siblings' flags set merges (it also clears those flags).  A
+ *                 call reads only what it wrote itself, apart from the flags; a stale flag is
+ *                 mistaken for this call's only if it holds exactly the call's 32-bit tag.
  *  rescale_count : optional device int32 [B, Hq, Sq] (NULL to skip).  The prefill kernel writes
  *                 for every query row how many times its softmax frame was moved (the first
  *                 key block always sets it, so every value is >= 1); the deferred rescale of
@@ -112,7 +116,9 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B,
                     void* workspace, size_t workspace_bytes, int32_t* rescale_count,
                     fa_stream_t stream);
 
-/* Scratch bytes fa_fwd_ex needs for this shape (0 for Sq >= 2). */
+/* Scratch bytes fa_fwd_ex needs for this shape on the current device (decode: the split
+ * partials; prefill: the partial rows of work units cut between CTAs, 0 when the launch runs
+ * one unit per CTA). */
 size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
                           int causal);
 

@@ -108,7 +108,10 @@ fa_status check_common(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_
 // decode scratch of one pair of cache formats (0 for Sq >= 2)
 size_t workspace_for(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
                      int causal, bool kq4, bool vq4, int* nsplit_out, int* chunk_out) {
-  if (Sq != 1) return 0;
+  if (Sq != 1)  // the cut schedule runs for dense K/V at D = 128
+    return (kq4 || vq4 || D != 128)
+               ? 0
+               : prefill_workspace_bytes(B, Hq, Sq, Sk, q_pos_offset, causal, D, num_sms());
   const int sk_eff = causal ? q_pos_offset + 1 : Sk;
   int ns = 1, ck = sk_eff;
   decode_plan(B, Hkv, sk_eff, num_sms(), kq4, vq4, &ns, &ck);
@@ -286,6 +289,10 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B,
   L.bf16 = bf16;
   L.kq4 = kq4;
   L.vq4 = vq4;
+  L.workspace = aligned16(workspace) ? workspace : nullptr;
+  L.workspace_bytes = L.workspace ? workspace_bytes : 0;
+  L.tag = next_call_tag();
+  L.num_sms = num_sms();
   return prefill_launch(L, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -16,8 +16,17 @@ struct PrefillLaunch {
   int B, Hq, Hkv, Sq, Sk, Scap, D, q_pos_offset, causal;  // Scap: K/V tokens per (b, kv head)
   float scale;
   bool bf16, kq4, vq4;
+  // scratch for the equal-cuts schedule (flags + partial rows; see prefill_workspace_bytes);
+  // with less than that the launch runs one work unit per CTA
+  void* workspace;
+  size_t workspace_bytes;
+  uint32_t tag;  // nonzero, different for every call
+  int num_sms;
 };
 cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream);
+// scratch the prefill launch needs to cut work units between CTAs (0: it runs whole units)
+size_t prefill_workspace_bytes(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causal,
+                               int D, int num_sms);
 uint32_t prefill_take_error();
 
 struct DecodeLaunch {

@@ -64,7 +64,7 @@ struct Cfg {
   static constexpr int kOffRing = kOffQ + 2 * kQBytes;
   static constexpr int kOffRaw = kOffRing + kStages * kTileBytes;
   static constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
-  static constexpr int kBarBytes = 512;
+  static constexpr int kBarBytes = 512 + 1024;  // barriers, flags, then the segment table
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   static constexpr int kWarps = 12;
   static constexpr int kThreads = kWarps * 32;
@@ -82,10 +82,18 @@ enum {
   kBarRingEmpty = 16,  // + stage
   kBarRawFull = 24,    // + raw stage
   kBarRawEmpty = 32,   // + raw stage
-  kBarCount = 40
+  kBarQEmpty = 40,     // the segment's last QK MMA has read the Q tiles (commit)
+  kBarOFree = 41,      // + tile (2): the segment's epilogue has read O out of TMEM (128 threads)
+  kBarPiece = 43,      // all 256 softmax threads have stored their rows of a piece
+  kBarMergeDecided = 44,  // the piece's flag is published and the merge decision made
+  kBarCount = 45
 };
 constexpr int kOffTmemSlot = kBarCount * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
+constexpr int kOffMergeFlag = kOffAbort + 8;
+constexpr int kOffSegCount = 512;        // within the barrier area: this CTA's segment count,
+constexpr int kOffSegs = kOffSegCount + 16;  // then its segments (SegS)
+constexpr int kMaxSegs = 16;
 
 struct PrefillArgs {
   void* o;
@@ -95,6 +103,13 @@ struct PrefillArgs {
   int B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, n_qtiles, n_pairs;
   int Scap;  // tokens per (batch, kv head) in the K/V tensors (row stride); Sk <= Scap
   float scale_log2;
+  // cut schedule (prefill_seg_kernel): W key-block steps in all, CTA c runs steps
+  // [range_start(c), range_start(c + 1))
+  int64_t W;
+  int n_ctas;
+  float* part;           // partial rows of units cut between CTAs (workspace), 2 slots per CTA
+  uint32_t* pflags;      // [n_ctas][2] publication flags (workspace), tagged per call
+  uint32_t tag;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -614,11 +629,781 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Cut schedule.  A work unit is a pair of consecutive 128-row query tiles (A, B) of one query
+// head; it takes nbmax steps, step j being key block j for both tiles.  Units are ordered by
+// pair (longest first), then batch, then head, and their steps concatenated; the sequence is cut
+// into equal contiguous ranges, one per resident CTA.  A CTA's range is a run of segments -- the
+// tail of one unit, whole units, the head of another -- so every SM does the same number of
+// steps and none idles through a last partial wave.  A unit cut between CTAs is finished by
+// whichever of its CTAs finds all its pieces published.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ int pair_steps(const PrefillArgs& a, int z) {
+  const int q0A = 2 * (a.n_pairs - 1 - z) * kBM;
+  return max(tile_blocks(a, q0A), tile_blocks(a, q0A + kBM));
+}
+
+struct Seg {
+  int b, h, g, q0A, q0B, nbA, nbB, nbmax, j0, j1;
+  bool hasB;
+  int64_t unit_start;  // global step of the unit's block 0
+};
+// a segment as stored in shared memory (computed once per CTA by one thread, read by every role)
+struct SegS {
+  int b, h, q0A, nbA, nbB, nbmax, j0, j1;
+  int64_t unit_start;
+};
+
+// the segment that starts at global step t of a range ending at t_end; false if t lies past
+// the last unit, which a consistent schedule never asks for
+__device__ __forceinline__ bool locate(const PrefillArgs& a, int64_t t, int64_t t_end, Seg& sg) {
+  const int64_t per_class = static_cast<int64_t>(a.B) * a.Hq;
+  int64_t acc = 0;
+  int z = 0;
+  int nbm = pair_steps(a, 0);
+  while (t >= acc + per_class * nbm) {
+    acc += per_class * nbm;
+    if (++z >= a.n_pairs || t < 0 || nbm <= 0) return false;
+    nbm = pair_steps(a, z);
+  }
+  if (nbm <= 0) return false;
+  const int64_t within = t - acc;
+  const int64_t idx = within / nbm;
+  sg.j0 = static_cast<int>(within - idx * nbm);
+  sg.b = static_cast<int>(idx / a.Hq);
+  sg.h = static_cast<int>(idx % a.Hq);
+  sg.g = sg.h / (a.Hq / a.Hkv);
+  sg.q0A = 2 * (a.n_pairs - 1 - z) * kBM;
+  sg.q0B = sg.q0A + kBM;
+  sg.nbA = tile_blocks(a, sg.q0A);
+  sg.nbB = tile_blocks(a, sg.q0B);
+  sg.nbmax = nbm;
+  sg.hasB = sg.q0B < a.Sq;
+  sg.unit_start = t - sg.j0;
+  sg.j1 = static_cast<int>(min(static_cast<int64_t>(nbm), sg.j0 + (t_end - t)));
+  return sg.j1 > sg.j0;
+}
+// first global step of CTA c's range (equal cuts)
+__device__ __forceinline__ int64_t range_start(const PrefillArgs& a, int c) {
+  return c >= a.n_ctas ? a.W : static_cast<int64_t>(c) * a.W / a.n_ctas;
+}
+// the CTA whose range holds global step t
+__device__ __forceinline__ int cta_of(const PrefillArgs& a, int64_t t) {
+  return static_cast<int>(((t + 1) * a.n_ctas - 1) / a.W);
+}
+// the same, and a piece's partial slot, on plain scalars (W steps over n CTAs): slot 0 when the
+// unit is where CTA c's range begins, 1 when the CTA reached it after other segments
+__device__ __forceinline__ int64_t cut_start(int c, int64_t W, int n) {
+  return c >= n ? W : static_cast<int64_t>(c) * W / n;
+}
+__device__ __forceinline__ int cut_cta_of(int64_t t, int64_t W, int n) {
+  return static_cast<int>(((t + 1) * n - 1) / W);
+}
+__device__ __forceinline__ int cut_slot(int c, int64_t unit_start, int64_t W, int n) {
+  return cut_start(c, W, n) >= unit_start ? 0 : 1;
+}
+// one tile of a piece, column-major so that a warp's 32 rows of one column are 128 contiguous
+// bytes: [D + 4 columns][128 rows] f32, columns O[0..D), frame, row sum, frame moves, pad
+template <int D>
+__device__ __forceinline__ float* part_tile(float* part, int c, int slot, int t) {
+  return part + ((static_cast<int64_t>(c) * 2 + slot) * 2 + t) * (D + 4) * kBM;
+}
+
+// record a schedule fault and stop the CTA's roles
+__device__ __forceinline__ void schedule_fault(volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicCAS(&g_prefill_error, kErrNone, kErrSchedule);
+}
+
+// Epilogue of one piece of a unit cut between CTAs, run by both tiles' softmax warps: store
+// this row's (O, frame, row sum, frame moves), release O, publish the piece's flag, and merge
+// all pieces if this CTA finds them all published.  Of two pieces published at the same time at
+// least one sees the other's flag (release store, then a sequentially consistent fence before
+// the flag loads), so at least one CTA merges; every CTA that does writes the same bytes.  Both
+// CTA-wide waits are bounded mbarriers.  Kept out of line: it runs a few times per CTA and would
+// otherwise take registers from the softmax loop.  Returns false if a bounded wait gave up.
+template <int D, bool BF16>
+__device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
+                                            uint32_t* pflags, uint32_t tag,
+                                            int32_t* rescale_count, void* o, int Hq, int Sq,
+                                            const SegS* sgp, uint32_t ocol, bool active, float f,
+                                            float l, int nres, uint32_t bar0, int pseg,
+                                            volatile int* abort_flag,
+                                            volatile uint32_t* merge_flag) {
+  // everything else follows from the thread and the segment (kept out of the caller's registers)
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int t = (warp >= 8) ? 1 : 0;
+  const int row = 32 * (warp & 3) + lane;
+  const int cta = static_cast<int>(blockIdx.x);
+  const int64_t unit_start = sgp->unit_start;
+  const int nbmax = sgp->nbmax;
+  const int qrow = sgp->q0A + t * kBM + row;
+  const bool exists = sgp->q0A + t * kBM < Sq;
+  const bool store = exists && qrow < Sq;
+  const int64_t orow_idx = static_cast<int64_t>(sgp->b * Hq + sgp->h) * Sq + qrow;
+  uint8_t* orow = static_cast<uint8_t*>(o) + orow_idx * D * 2;
+  const int slot = cut_slot(cta, unit_start, W, n_ctas);
+  if (exists) {
+    float* pt = part_tile<D>(part, cta, slot, t) + row;
+    if (active) {
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(ocol + 32 * c, r);
+        tmem_wait_ld();
+        reg_fence32(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pt[(32 * c + i) * kBM] = __uint_as_float(r[i]);
+      }
+    }
+    pt[D * kBM] = active ? f : -INFINITY;
+    pt[(D + 1) * kBM] = active ? l : 0.f;
+    pt[(D + 2) * kBM] = __int_as_float(active ? nres : 0);
+  }
+  if (active) {
+    // O has been read out of tensor memory: the next segment's PV may overwrite it
+    tc_fence_before();
+    mbar_arrive(bar0 + 8u * (kBarOFree + t));
+  }
+  const int c_first = cut_cta_of(unit_start, W, n_ctas);
+  const int c_last = cut_cta_of(unit_start + nbmax - 1, W, n_ctas);
+  mbar_arrive(bar0 + 8u * kBarPiece);
+  if (warp == 4) {
+    bool okw = mbar_wait(bar0 + 8u * kBarPiece, pseg & 1, abort_flag, &g_prefill_error);
+    okw = __all_sync(0xffffffffu, okw);
+    bool all = false;
+    if (okw) {
+      if (lane == 0) st_release_gpu(pflags + 2 * cta + slot, tag);
+      __syncwarp();
+      fence_sc_gpu();
+      all = true;
+      for (int c = c_first + lane; c <= c_last; c += 32)
+        all = all && ld_relaxed_gpu(pflags + 2 * c + cut_slot(c, unit_start, W, n_ctas)) == tag;
+      all = __all_sync(0xffffffffu, all);
+      if (all) fence_acq_rel_gpu();
+    }
+    if (lane == 0) {
+      *merge_flag = all ? 1u : 0u;
+      mbar_arrive(bar0 + 8u * kBarMergeDecided);
+    }
+  }
+  const bool ok = mbar_wait(bar0 + 8u * kBarMergeDecided, pseg & 1, abort_flag, &g_prefill_error);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  const bool merge = *merge_flag != 0u;
+  if (merge && exists) {
+    // frame F = max over the pieces, weights 2^(f_p - F), pieces in CTA order
+    auto tile_of = [&](int c) -> const float* {
+      return part_tile<D>(part, c, cut_slot(c, unit_start, W, n_ctas), t) + row;
+    };
+    float F = -INFINITY;
+    for (int c = c_first; c <= c_last; ++c) F = fmaxf(F, __ldcg(tile_of(c) + D * kBM));
+    // frame moves: each piece counts its own first frame; the row as a whole counts one
+    float L = 0.f;
+    int moves = 1;
+    for (int c = c_first; c <= c_last; ++c) {
+      const float* pc = tile_of(c);
+      const float fp = __ldcg(pc + D * kBM);
+      if (fp == -INFINITY) continue;
+      L = fmaf(ex2(fp - F), __ldcg(pc + (D + 1) * kBM), L);
+      moves += __float_as_int(__ldcg(pc + (D + 2) * kBM)) - 1;
+    }
+    const float inv_l = 1.f / L;
+#pragma unroll 1
+    for (int cc = 0; cc < D / 16; ++cc) {
+      float acc[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+      for (int c = c_first; c <= c_last; ++c) {
+        const float* pc = tile_of(c);
+        const float fp = __ldcg(pc + D * kBM);
+        if (fp == -INFINITY) continue;
+        const float w = ex2(fp - F);
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __ldcg(pc + (16 * cc + i) * kBM);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+      }
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pk[i] = pack2<BF16>(acc[2 * i] * inv_l, acc[2 * i + 1] * inv_l);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+    if (store && rescale_count) rescale_count[orow_idx] = moves;
+  }
+  if (merge && warp == 4) {
+    // clear the unit's flags for the next call (or graph replay) with this tag
+    for (int c = c_first + lane; c <= c_last; c += 32)
+      st_relaxed_gpu(pflags + 2 * c + cut_slot(c, unit_start, W, n_ctas), 0u);
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------------------------------
+// The same kernel run over segments of work units (the equal-cuts schedule below): every role
+// walks this CTA's segments, a unit cut between CTAs is published as partial rows and merged by
+// its last piece.  Used where cutting beats one unit per CTA (more units than SMs, long units).
+// ------------------------------------------------------------------------------------------
+template <int D, bool BF16, bool KQ4, bool VQ4>
+__global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
+    prefill_seg_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
+  using C = Cfg<D, KQ4, VQ4>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffBar + kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::kOffBar + kOffTmemSlot);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // this CTA's run of key-block steps, an equal cut of all units' steps; each role walks the
+  // same segments (see the cut schedule above).  Tile B of a unit may lie past
+  // Sq (odd tile count); causal rows further down see at least as many keys, so nbmax = nbB
+  // whenever tile B exists.
+  const int cta = static_cast<int>(blockIdx.x);
+  const int64_t t_begin = range_start(args, cta);
+  const int64_t t_end = range_start(args, cta + 1);
+  volatile int* seg_count = reinterpret_cast<volatile int*>(sgen + C::kOffBar + kOffSegCount);
+  SegS* segs = reinterpret_cast<SegS*>(sgen + C::kOffBar + kOffSegs);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQFull), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kBarSFull + t), 1);
+      mbar_init(bar(kBarPReady + t), 128);
+      mbar_init(bar(kBarODone + t), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarQEmpty), 1);
+    mbar_init(bar(kBarOFree + 0), 128);
+    mbar_init(bar(kBarOFree + 1), 128);
+    mbar_init(bar(kBarPiece), 256);
+    mbar_init(bar(kBarMergeDecided), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      // a q4_0 stage is filled by the 64 dequant threads, a dense one by the TMA lane
+      const bool q4s = (C::kStages % 2 == 0) ? ((s & 1) ? VQ4 : KQ4) : (KQ4 && VQ4);
+      mbar_init(bar(kBarRingFull + s), q4s ? 64 : 1);
+      mbar_init(bar(kBarRingEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kRawStages; ++s) {
+      mbar_init(bar(kBarRawFull + s), 1 + 32);  // TMA lane + 32 cp.async arrivals
+      mbar_init(bar(kBarRawEmpty + s), 64);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    // this CTA's segments, once: the roles read them back instead of each locating them
+    int ns = 0;
+    for (int64_t tt = t_begin; tt < t_end;) {
+      Seg sg;
+      if (ns >= kMaxSegs || !locate(args, tt, t_end, sg)) {
+        schedule_fault(abort_flag);
+        ns = 0;
+        break;
+      }
+      segs[ns] = SegS{sg.b, sg.h, sg.q0A, sg.nbA, sg.nbB, sg.nbmax, sg.j0, sg.j1, sg.unit_start};
+      ++ns;
+      tt += sg.j1 - sg.j0;
+    }
+    *seg_count = ns;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nseg = *seg_count;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+    }
+    bool ok = true;
+    // tiles in the order the MMA first uses them: K0, V0, K1, V1, ... of each segment; dense
+    // tiles go by TMA straight into the ring, q4_0 tiles (nibbles + scales) into the raw stages
+    int n = 0;   // ring tiles
+    int r = 0;   // raw q4_0 tiles
+    int qn = 0;  // Q loads issued
+    int b = 0, g = 0;  // the segment's batch and kv head
+    auto produce = [&](bool is_v, int j) {
+      if (!ok) return;
+      if (!(is_v ? VQ4 : KQ4)) {
+        const int s = n % C::kStages;
+        if (lane == 0) {
+          if (n >= C::kStages)
+            ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                           &g_prefill_error);
+          if (ok) {
+            mbar_arrive_expect_tx(bar(kBarRingFull + s), C::kTileBytes);
+            const uint32_t dst = sbase + C::kOffRing + s * C::kTileBytes;
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(dst + c * (kBN * 128), is_v ? &tm_v : &tm_k, bar(kBarRingFull + s),
+                          c * 64, j * kBN, b * args.Hkv + g);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      } else {
+        const int s = r % C::kRawStages;
+        if (r >= C::kRawStages) {
+          if (lane == 0)
+            ok = mbar_wait(bar(kBarRawEmpty + s), ((r / C::kRawStages) - 1) & 1, abort_flag,
+                           &g_prefill_error);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) return;
+        }
+        const uint32_t dst = sbase + C::kOffRaw + s * C::kRawBytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(kBarRawFull + s), C::kRawNib);
+          tma_load_3d(dst, is_v ? &tm_v : &tm_k, bar(kBarRawFull + s), 0, j * kBN,
+                      b * args.Hkv + g);
+        }
+        // scales: one 4- or 8-byte row per key, zero-filled past Sk
+        const uint8_t* sp = is_v ? args.v_scale : args.k_scale;
+        for (int row = lane; row < kBN; row += 32) {
+          const int key = j * kBN + row;
+          const bool in = key < args.Sk;
+          const uint8_t* src =
+              sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Scap + (in ? key : 0)) *
+                       C::kScaleRow;
+          const uint32_t d = dst + C::kRawNib + row * C::kScaleRow;
+          if (C::kScaleRow == 8)
+            cp_async_8(d, src, in ? 8u : 0u);
+          else
+            cp_async_4(d, src, in ? 4u : 0u);
+        }
+        cp_async_mbar_arrive_noinc(bar(kBarRawFull + s));
+        ++r;
+      }
+      ++n;
+    };
+    for (int sidx = 0; sidx < nseg && ok; ++sidx) {
+      const SegS sg = segs[sidx];
+      const bool hasB = sg.q0A + kBM < args.Sq;
+      b = sg.b;
+      g = sg.h / (args.Hq / args.Hkv);
+      // the segment's Q tiles, once the previous segment's last QK MMA has read the previous ones
+      if (lane == 0) {
+        if (sidx > 0)
+          ok = mbar_wait(bar(kBarQEmpty), (sidx - 1) & 1, abort_flag, &g_prefill_error);
+        if (ok) {
+          mbar_arrive_expect_tx(bar(kBarQFull), (hasB ? 2 : 1) * C::kQBytes);
+          for (int t = 0; t < (hasB ? 2 : 1); ++t)
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (kBM * 128), &tm_q,
+                          bar(kBarQFull), c * 64, sg.q0A + t * kBM, sg.b * args.Hq + sg.h);
+          ++qn;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      for (int j = sg.j0; j < sg.j1; ++j) {
+        produce(false, j);
+        produce(true, j);
+      }
+    }
+    if (!ok && lane == 0) {
+      // let copies already issued land before the CTA's shared memory goes away: the last
+      // Q tiles, the last dense tiles sent into the ring and the last raw q4_0 tiles
+      volatile int never = 0;
+      if (qn > 0)
+        mbar_wait(bar(kBarQFull), (qn - 1) & 1, &never, nullptr, kWaitLimitNs);
+      for (int i = max(0, n - C::kStages); i < n; ++i)
+        if (!((i & 1) ? VQ4 : KQ4))
+          mbar_wait(bar(kBarRingFull + i % C::kStages), (i / C::kStages) & 1, &never, nullptr,
+                    kWaitLimitNs);
+      if constexpr (C::kAnyQ4) {
+        for (int i = max(0, r - C::kRawStages); i < r; ++i)
+          mbar_wait(bar(kBarRawFull + i % C::kRawStages), (i / C::kRawStages) & 1, &never,
+                    nullptr, kWaitLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc_f16(kBM, kBN, BF16, false);
+      constexpr uint32_t idesc_pv = make_idesc_f16(kBM, D, BF16, true);
+      bool ok = true;
+      int n = 0;
+      int prA = 0, prB = 0;    // P-ready waits per tile before this segment (barrier phases)
+      int actA = 0, actB = 0;  // earlier segments in which the tile had blocks
+      auto acquire = [&]() -> int {
+        const int s = n % C::kStages;
+        if (ok) ok = mbar_wait(bar(kBarRingFull + s), (n / C::kStages) & 1, abort_flag,
+                               &g_prefill_error);
+        tc_fence_after();
+        ++n;
+        return s;
+      };
+      auto release = [&](int s) { mma_commit(bar(kBarRingEmpty + s)); };
+      auto issue_qk = [&](int t, int s) {
+        const uint32_t qaddr = sbase + C::kOffQ + t * C::kQBytes;
+        const uint32_t kaddr = sbase + C::kOffRing + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          mma_ss(tmem + col_s(t), make_sdesc_sw128(qaddr + off, 16, 1024),
+                 make_sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kBarSFull + t));
+      };
+      // PV of tile t for block j of a segment whose blocks for t are [j0, e_t); pr0 = the
+      // tile's P-ready waits before the segment, act = its earlier segments with blocks
+      auto issue_pv = [&](int t, int j, int s, int j0, int e_t, int pr0, int act) {
+        if (j == j0 && act > 0)  // the previous segment's epilogue has read O
+          ok = ok && mbar_wait(bar(kBarOFree + t), (act - 1) & 1, abort_flag, &g_prefill_error);
+        ok = ok && mbar_wait(bar(kBarPReady + t), (pr0 + j - j0) & 1, abort_flag,
+                             &g_prefill_error);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
+        const uint32_t ocol = t ? C::kColO1 : C::kColO0;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + ocol, tmem + col_s(t) + kk * 8,
+                 make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
+                 (j > j0 || kk > 0) ? 1u : 0u);
+        if (j == e_t - 1) mma_commit(bar(kBarODone + t));
+      };
+      // per segment: QK_A(j0) QK_B(j0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage
+      // is acquired at the start of the step that first uses it and released after its last use
+      // (all in ring order).  Both ring waits of a step sit next to the P_A wait: an mbarrier
+      // wait issued while the MMA queue is short stalls the issue of the next MMAs, so the waits
+      // are grouped where they cost one stall instead of one per wait.
+      for (int sidx = 0; sidx < nseg && ok; ++sidx) {
+        const int j0 = segs[sidx].j0, j1 = segs[sidx].j1;
+        const int eA = min(j1, segs[sidx].nbA);
+        const int eB = segs[sidx].q0A + kBM < args.Sq ? min(j1, segs[sidx].nbB) : 0;
+        ok = mbar_wait(bar(kBarQFull), sidx & 1, abort_flag, &g_prefill_error);
+        tc_fence_after();
+        if (!ok) break;
+        {
+          const int sK = acquire();
+          if (!ok) break;
+          if (j0 < eA) issue_qk(0, sK);
+          if (j0 < eB) issue_qk(1, sK);
+          release(sK);
+          if (j0 + 1 == j1) mma_commit(bar(kBarQEmpty));  // no further QK reads these Q tiles
+        }
+        for (int j = j0; j < j1 && ok; ++j) {
+          const int sV = acquire();
+          const bool next = j + 1 < j1;
+          const int sK = next ? acquire() : 0;
+          if (!ok) break;
+          if (j < eA) issue_pv(0, j, sV, j0, eA, prA, actA);
+          if (!ok) break;
+          if (next && j + 1 < eA) issue_qk(0, sK);
+          if (j < eB) issue_pv(1, j, sV, j0, eB, prB, actB);
+          if (!ok) break;
+          release(sV);
+          if (next) {
+            if (j + 1 < eB) issue_qk(1, sK);
+            release(sK);
+            if (j + 2 == j1) mma_commit(bar(kBarQEmpty));
+          }
+        }
+        if (j0 < eA) {
+          ++actA;
+          prA += eA - j0;
+        }
+        if (j0 < eB) {
+          ++actB;
+          prB += eB - j0;
+        }
+      }
+      if (!ok) {
+        // wait until every MMA issued so far has finished before TMEM is released
+        volatile int never = 0;
+        mma_commit(bar(kBarDrain));
+        mbar_wait(bar(kBarDrain), 0, &never, nullptr, kWaitLimitNs);
+      }
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------------------------------------------------------- softmax rows
+    const int t = (warp >= 8) ? 1 : 0;  // query tile
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t scol = tmem + lane_off + col_s(t);
+    const uint32_t ocol = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
+    const float sl2 = args.scale_log2;
+    volatile uint32_t* merge_flag =
+        reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + kOffMergeFlag);
+    bool ok = true;
+    int sf = 0;    // S-full waits so far (barrier phase)
+    int od = 0;    // segments in which this tile had blocks (O-done phase)
+    int pseg = 0;  // pieces published so far
+    for (int sidx = 0; sidx < nseg && ok; ++sidx) {
+      // only what the block loop needs is read before it; the rest after it
+      const int j0 = segs[sidx].j0;
+      const int q0 = segs[sidx].q0A + t * kBM;
+      const int e_t = q0 < args.Sq ? min(segs[sidx].j1, t ? segs[sidx].nbB : segs[sidx].nbA) : 0;
+      const int pos = args.q_pos_offset + q0 + row;
+      float f = -INFINITY;  // frame, base-2 units of the scaled score
+      float l = 0.f;
+      int nres = 0;
+      for (int j = j0; j < e_t; ++j) {
+        ok = mbar_wait(bar(kBarSFull + t), sf & 1, abort_flag, &g_prefill_error);
+        ++sf;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int kb = j * kBN;
+        const bool need_mask =
+            (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
+        // last visible key of this row, relative to the block
+        const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
+        // pass 1: row max over the 128 scores
+        const float mx = need_mask ? block_row_max<true>(scol, rel_lim)
+                                   : block_row_max<false>(scol, rel_lim);
+        const float m2 = mx * sl2;
+        const bool need = m2 > f + kMarginLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2(f - m2) : 1.f;
+          if (need) {
+            l *= alpha;
+            f = m2;
+            ++nres;
+          }
+          // S(j) being ready means PV(j-1) has completed (QK(j) was issued after it), so O can be
+          // rescaled in place without a further wait (j > j0: O holds this segment's blocks)
+          if (j > j0) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(ocol + 32 * c, r);
+              tmem_wait_ld();
+              reg_fence32(r);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tmem_st32(ocol + 32 * c, r);
+            }
+            tmem_wait_st();
+          }
+        }
+        // pass 2: P = 2^(t - f) over the first half of S, row sum
+        const float nf = -f;
+        l += need_mask ? block_row_exp<true, BF16>(scol, rel_lim, sl2, nf)
+                       : block_row_exp<false, BF16>(scol, rel_lim, sl2, nf);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPReady + t));
+      }
+      if (!ok) break;
+      const SegS sg = segs[sidx];
+      const bool exists = q0 < args.Sq;
+      const bool active = e_t > j0;  // the tile had key blocks in this segment
+      const int qrow = q0 + row;
+      if (active) {
+        // the tile's last PV MMA of the segment completing implies all of its MMAs have
+        ok = mbar_wait(bar(kBarODone + t), od & 1, abort_flag, &g_prefill_error);
+        ++od;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const bool store = exists && qrow < args.Sq;
+      const int64_t orow_idx = static_cast<int64_t>(sg.b * args.Hq + sg.h) * args.Sq + qrow;
+      uint8_t* orow = static_cast<uint8_t*>(args.o) + orow_idx * D * 2;
+      const bool split = cta_of(args, sg.unit_start) != cta_of(args, sg.unit_start + sg.nbmax - 1);
+      if (!split) {
+        if (active) {
+          const float inv_l = 1.f / l;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(ocol + 32 * c, r);
+            tmem_wait_ld();
+            reg_fence32(r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv_l,
+                                  __uint_as_float(r[2 * i + 1]) * inv_l);
+            if (store) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+          if (store && args.rescale_count) args.rescale_count[orow_idx] = nres;
+          // O has been read out of tensor memory: the next segment's PV may overwrite it
+          tc_fence_before();
+          mbar_arrive(bar(kBarOFree + t));
+        }
+      } else {
+        ok = piece_epilogue<D, BF16>(args.W, args.n_ctas, args.part, args.pflags, args.tag,
+                                     args.rescale_count, args.o, args.Hq, args.Sq, segs + sidx,
+                                     ocol, active, f, l, nres, bar0, pseg, abort_flag,
+                                     merge_flag);
+        ++pseg;
+      }
+    }
+  } else if constexpr (C::kAnyQ4) {
+    if (warp == 2 || warp == 3) {
+      // -------------------------------------------------------------- q4_0 dequant
+      // thread u expands key rows u and u + 64 of each raw tile into the 128B-swizzled
+      // f16/bf16 ring stage
+      const int u = threadIdx.x - 2 * 32;
+      const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
+      bool ok = true;
+      const int ntiles = static_cast<int>(2 * (t_end - t_begin));  // K and V of every step
+      int r = 0;  // raw q4_0 tiles consumed
+      for (int n = 0; n < ntiles; ++n) {
+        if (!((n & 1) ? VQ4 : KQ4)) continue;  // a dense tile: the producer's TMA fills it
+        const int rs = r % C::kRawStages;
+        const int s = n % C::kStages;
+        ok = mbar_wait(bar(kBarRawFull + rs), (r / C::kRawStages) & 1, abort_flag,
+                       &g_prefill_error);
+        if (ok && n >= C::kStages)
+          ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                         &g_prefill_error);
+        if (!ok) break;
+        const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
+        uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
+#pragma unroll 1
+        for (int rr = 0; rr < 2; ++rr) {
+        const int t = u + 64 * rr;  // key row within the tile
+        const uint8_t* nrow = raw + t * C::kNibRow;
+        const __half* srow =
+            reinterpret_cast<const __half*>(raw + C::kRawNib + t * C::kScaleRow);
+#pragma unroll
+        for (int blk = 0; blk < D / 32; ++blk) {
+          // 16 bytes of nibbles of this key, 64B-swizzled (D=128) or 32B-swizzled (D=64)
+          const int chunk = (D == 128) ? (blk ^ ((t >> 1) & 3)) : (blk ^ ((t >> 2) & 1));
+          const uint4 wv = *reinterpret_cast<const uint4*>(nrow + 16 * chunk);
+          const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+          const __half dh = srow[blk];
+          uint32_t outv[16];  // 32 dequantized elements, packed in pairs, natural order
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            // bytes 4q..4q+3 -> elements 4q..4q+3 (low) and 4q+16..4q+19 (high)
+            const uint32_t a = __byte_perm(w[q], 0u, 0x5150);   // byte0 at b0, byte1 at b2
+            const uint32_t c2 = __byte_perm(w[q], 0u, 0x5352);  // byte2 at b0, byte3 at b2
+            if (BF16) {
+              const float d = __half2float(dh);
+              outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a, mg), d);
+              outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2, mg), d);
+              outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a, mg), d);
+              outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2, mg), d);
+            } else {
+              outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a, mg), dh);
+              outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2, mg), dh);
+              outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a, mg), dh);
+              outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2, mg), dh);
+            }
+          }
+          // elements 32 blk + 8 cc .. +7 form 16-byte chunk (4 blk + cc) of the row
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int col16 = 4 * blk + cc;        // 16-byte chunk index along D
+            const int atom = col16 >> 3;           // 64-element swizzle atom
+            const int ch = (col16 & 7) ^ (t & 7);  // 128B swizzle
+            *reinterpret_cast<uint4*>(dst + atom * (kBN * 128) + t * 128 + ch * 16) =
+                make_uint4(outv[4 * cc], outv[4 * cc + 1], outv[4 * cc + 2], outv[4 * cc + 3]);
+          }
+        }
+        }
+        // generic-proxy writes must be visible to the tensor core's async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(bar(kBarRingFull + s));
+        mbar_arrive(bar(kBarRawEmpty + rs));
+        ++r;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------------------------------
 // host launch
 // ------------------------------------------------------------------------------------------
+// The schedule of a launch: W key-block steps over `units` work units; equal cuts over n_ctas
+// resident CTAs (one per SM) when that is estimated to finish sooner than one unit per CTA,
+// else one unit per CTA.  Estimates in steps: one unit per CTA takes ceil(units / SMs) waves of
+// an average unit; equal cuts take W / SMs steps plus ~8 steps per segment boundary (the Q
+// reload, the epilogue, the partial write and merge, measured at 16K keys).
+struct Plan {
+  int64_t W, units;
+  int n_ctas;
+  bool whole;
+  size_t flag_bytes, bytes;
+};
+static Plan make_plan(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causal, int D,
+                      int num_sms) {
+  auto blocks = [&](int q0) -> int64_t {  // the device's tile_blocks, on the host
+    if (q0 >= Sq) return 0;
+    const int last_row = q0 + kBM - 1 < Sq - 1 ? q0 + kBM - 1 : Sq - 1;
+    const int64_t kend = causal ? (Sk < static_cast<int64_t>(q_pos_offset) + last_row + 1
+                                       ? Sk
+                                       : static_cast<int64_t>(q_pos_offset) + last_row + 1)
+                                : Sk;
+    return (kend + kBN - 1) / kBN;
+  };
+  const int n_qtiles = (Sq + kBM - 1) / kBM;
+  const int n_pairs = (n_qtiles + 1) / 2;
+  const int64_t per_class = static_cast<int64_t>(B) * Hq;
+  Plan p;
+  p.units = per_class * n_pairs;
+  p.W = 0;
+  int64_t nb_min = 0;  // the shortest unit
+  for (int z = 0; z < n_pairs; ++z) {
+    const int q0A = 2 * (n_pairs - 1 - z) * kBM;
+    const int64_t a = blocks(q0A), b = blocks(q0A + kBM);
+    const int64_t nb = a > b ? a : b;
+    p.W += per_class * nb;
+    if (z == 0 || nb < nb_min) nb_min = nb;
+  }
+  // a CTA's range spans at most ceil(steps / nb_min) + 2 segments, which must fit its table
+  const int64_t per_cta = num_sms > 0 ? (p.W + num_sms - 1) / num_sms : 0;
+  const bool fits = nb_min > 0 && (per_cta + nb_min - 1) / nb_min + 2 <= kMaxSegs;
+  bool cuts = num_sms > 0 && p.units > num_sms && fits;
+  if (cuts) {
+    const double avg = static_cast<double>(p.W) / static_cast<double>(p.units);
+    const double whole_est = static_cast<double>((p.units + num_sms - 1) / num_sms) * avg;
+    const double cut_est = static_cast<double>(per_cta) + 8.0 * (per_cta / avg + 1.0);
+    cuts = cut_est < 0.97 * whole_est;
+  }
+  p.whole = !cuts;
+  p.n_ctas = p.whole ? 0 : num_sms;
+  p.flag_bytes = p.whole ? 0 : (static_cast<size_t>(p.n_ctas) * 2 * sizeof(uint32_t) + 255) /
+                                   256 * 256;
+  p.bytes = p.whole ? 0
+                    : p.flag_bytes + static_cast<size_t>(p.n_ctas) * 2 * 2 * (D + 4) * kBM *
+                                         sizeof(float);
+  return p;
+}
+
+size_t prefill_workspace_bytes(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causal,
+                               int D, int num_sms) {
+  return make_plan(B, Hq, Sq, Sk, causal ? q_pos_offset : 0, causal, D, num_sms).bytes;
+}
+
 template <int D, bool BF16, bool KQ4, bool VQ4>
 static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   using C = Cfg<D, KQ4, VQ4>;
@@ -643,6 +1428,11 @@ static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   a.n_qtiles = (L.Sq + kBM - 1) / kBM;
   a.n_pairs = (a.n_qtiles + 1) / 2;
   a.scale_log2 = L.scale * kLog2e;
+  a.W = 0;  // one unit per CTA from the grid coordinates; the cut-schedule fields are unused
+  a.n_ctas = 0;
+  a.part = nullptr;
+  a.pflags = nullptr;
+  a.tag = 0;
   dim3 grid(L.Hq, L.B, a.n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, a);
   return cudaGetLastError();
@@ -656,7 +1446,45 @@ static cudaError_t launch_fmt(const PrefillLaunch& L, cudaStream_t stream) {
                : launch_t<D, BF16, false, false>(L, stream);
 }
 
+// equal cuts of the step sequence over one CTA per SM (dense K/V, D = 128)
+template <bool BF16>
+static cudaError_t launch_seg(const PrefillLaunch& L, const Plan& p, cudaStream_t stream) {
+  using C = Cfg<128, false, false>;
+  auto kern = prefill_seg_kernel<128, BF16, false, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  PrefillArgs a;
+  a.o = L.o;
+  a.k_scale = nullptr;
+  a.v_scale = nullptr;
+  a.rescale_count = L.rescale_count;
+  a.B = L.B;
+  a.Hq = L.Hq;
+  a.Hkv = L.Hkv;
+  a.Sq = L.Sq;
+  a.Sk = L.Sk;
+  a.Scap = L.Scap;
+  a.q_pos_offset = L.q_pos_offset;
+  a.causal = L.causal;
+  a.n_qtiles = (L.Sq + kBM - 1) / kBM;
+  a.n_pairs = (a.n_qtiles + 1) / 2;
+  a.scale_log2 = L.scale * kLog2e;
+  a.W = p.W;
+  a.n_ctas = p.n_ctas;
+  a.pflags = static_cast<uint32_t*>(L.workspace);
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(L.workspace) + p.flag_bytes);
+  a.tag = L.tag;
+  kern<<<dim3(a.n_ctas), C::kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, a);
+  return cudaGetLastError();
+}
+
 cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream) {
+  if (L.D == 128 && !L.kq4 && !L.vq4) {
+    const Plan p = make_plan(L.B, L.Hq, L.Sq, L.Sk, L.q_pos_offset, L.causal, L.D, L.num_sms);
+    if (!p.whole && L.workspace != nullptr && L.workspace_bytes >= p.bytes)
+      return L.bf16 ? launch_seg<true>(L, p, stream) : launch_seg<false>(L, p, stream);
+  }
   if (L.D == 128)
     return L.bf16 ? launch_fmt<128, true>(L, stream) : launch_fmt<128, false>(L, stream);
   return L.bf16 ? launch_fmt<64, true>(L, stream) : launch_fmt<64, false>(L, stream);

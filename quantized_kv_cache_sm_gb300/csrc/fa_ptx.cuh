@@ -17,6 +17,7 @@ enum : uint32_t {
   kErrNone = 0,
   kErrTimeout = 1,  // a bounded wait ran out
   kErrBadIndex = 2,  // a device-side index input (page number, sequence length) was out of range
+  kErrSchedule = 3,  // a CTA's work range did not map onto the work units (inconsistent plan)
 };
 
 // A wait that has not completed after this long is treated as a hang (the longest legitimate

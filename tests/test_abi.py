@@ -6,6 +6,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 import quantized_kv_cache_sm_gb300 as fa
 from quantized_kv_cache_sm_gb300 import build as fa_build
@@ -57,7 +58,11 @@ def test_q4_0_sizes(lib):
     assert fa.fa_q4_0_bytes(1, 1, 1, 48) == 0  # D must be a multiple of 32
 
 
-def test_workspace_is_zero_for_prefill(lib):
+def test_prefill_workspace_without_a_device(lib):
+    # the prefill schedule is planned for the current device's SM count; with no device the plan
+    # runs one work unit per CTA, which needs no scratch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
     assert fa.fa_workspace_bytes(1, 32, 8, 2048, 16384, 128, 14336, 1) == 0
     assert fa.fa_workspace_bytes(1, 32, 7, 2, 16, 128, 0, 1) == 0  # invalid: Hq % Hkv
 
