@@ -108,3 +108,31 @@ def test_cut_schedule_stale_workspace_and_graph_replay(fa):
         torch.cuda.synchronize()
         assert torch.equal(os_, eager), seed
     assert fa.fa_get_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("shape", [
+    # B, Hq, Hkv, Sq, Sk, causal, dtype: 160 units (odd tile count: the last pair of every head
+    # has no tile B), ragged Sq and Sk, two batches
+    (2, 16, 4, 1152, 20000, True, "f16"),
+    # non-causal, 192 units of 64 steps, last pair of every head without tile B
+    (1, 64, 8, 640, 8192, False, "bf16"),
+], ids=lambda c: "-".join(map(str, c)))
+def test_cut_schedule_other_shapes(fa, shape):
+    B, Hq, Hkv, Sq, Sk, causal, dtype = shape
+    off = Sk - Sq if causal else 0
+    n = fa.fa_workspace_bytes(B, Hq, Hkv, Sq, Sk, 128, off, causal)
+    units = B * Hq * ((Sq + 255) // 256)
+    if torch.cuda.get_device_properties(0).multi_processor_count < units:
+        assert n > 0, "no cut schedule planned"
+    q, k, v = fa_inputs.make_tensors(B, Hq, Hkv, Sq, Sk, 128, dtype, seed=Sq + Sk)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    o_cut = fa.fa_fwd_ex(qd, kd, vd, causal=causal, q_pos_offset=off, workspace=ws)
+    o_whole = fa.fa_fwd_ex(qd, kd, vd, causal=causal, q_pos_offset=off)
+    assert fa.fa_get_status() == fa.FA_OK
+    rows = sample_rows(B, Hq, Sq, per_head=8, seed=3)
+    want = oracle.attention(np64(q), np64(k), np64(v), causal=causal, q_pos_offset=off,
+                            scale=128 ** -0.5, rows=rows)
+    check_close(np64(o_cut).reshape(-1, 128)[rows], want, dtype, f"{shape} cut schedule")
+    diff = (o_cut.float() - o_whole.float()).abs().max().item()
+    assert diff <= (4e-3 if dtype == "f16" else 3e-2), diff
