@@ -1060,13 +1060,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         }
         mma_commit(bar(kBarSFull + t));
       };
-      // PV of tile t for block j of a segment whose blocks for t are [j0, e_t); pr0 = the
-      // tile's P-ready waits before the segment, act = its earlier segments with blocks
-      auto issue_pv = [&](int t, int j, int s, int j0, int e_t, int pr0, int act) {
-        if (j == j0 && act > 0)  // the previous segment's epilogue has read O
-          ok = ok && mbar_wait(bar(kBarOFree + t), (act - 1) & 1, abort_flag, &g_prefill_error);
-        ok = ok && mbar_wait(bar(kBarPReady + t), (pr0 + j - j0) & 1, abort_flag,
-                             &g_prefill_error);
+      // PV of tile t for block j of a segment whose blocks for t are [j0, e_t); the P-ready
+      // phase of block j is (pb + j) & 1, pb = the tile's earlier P-ready waits - j0
+      auto issue_pv = [&](int t, int j, int s, int j0, int e_t, int pb) {
+        ok = ok && mbar_wait(bar(kBarPReady + t), (pb + j) & 1, abort_flag, &g_prefill_error);
         if (!ok) return;
         tc_fence_after();
         const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
@@ -1098,15 +1095,22 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           release(sK);
           if (j0 + 1 == j1) mma_commit(bar(kBarQEmpty));  // no further QK reads these Q tiles
         }
+        // a tile's first PV of the segment overwrites O: wait until the previous segment's
+        // epilogue has read it (after this segment's first QKs are on their way)
+        if (j0 < eA && actA > 0)
+          ok = ok && mbar_wait(bar(kBarOFree + 0), (actA - 1) & 1, abort_flag, &g_prefill_error);
+        if (j0 < eB && actB > 0)
+          ok = ok && mbar_wait(bar(kBarOFree + 1), (actB - 1) & 1, abort_flag, &g_prefill_error);
+        const int pbA = prA - j0, pbB = prB - j0;
         for (int j = j0; j < j1 && ok; ++j) {
           const int sV = acquire();
           const bool next = j + 1 < j1;
           const int sK = next ? acquire() : 0;
           if (!ok) break;
-          if (j < eA) issue_pv(0, j, sV, j0, eA, prA, actA);
+          if (j < eA) issue_pv(0, j, sV, j0, eA, pbA);
           if (!ok) break;
           if (next && j + 1 < eA) issue_qk(0, sK);
-          if (j < eB) issue_pv(1, j, sV, j0, eB, prB, actB);
+          if (j < eB) issue_pv(1, j, sV, j0, eB, pbB);
           if (!ok) break;
           release(sV);
           if (next) {
