@@ -207,12 +207,11 @@ def run_ours(args, rank, world, local_rank):
         k, v = fa.fa_quantize_q4_0(k), fa.fa_quantize_q4_0(v)
     o = torch.empty_like(q)
     rc = None
-    # scratch: the decode partials, or the prefill's cut schedule (dense K/V, D = 128) where the
+    # scratch: the decode partials, or the prefill's cut schedule (D = 128) where the
     # library plans one for this device; without it the prefill runs one work unit per CTA
     n_ws = fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset, w.causal)
     ws = torch.empty(n_ws, dtype=torch.uint8, device=dev) if n_ws > 0 else None
-    kernel = ("prefill_seg_kernel" if w.Sq > 1 and n_ws > 0 and w.kv_format == "dense"
-              and w.D == 128 else "prefill_kernel")
+    kernel = "prefill_seg_kernel" if w.Sq > 1 and n_ws > 0 and w.D == 128 else "prefill_kernel"
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 

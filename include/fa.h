@@ -73,7 +73,7 @@ typedef enum {
  * fa_fwd takes it from the stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on `stream`);
  * use fa_fwd_ex to pass one instead.  Sq >= 2 runs the prefill kernel; where there are more
  * work units than SMs and cutting them evenly over one CTA per SM is estimated to finish sooner
- * (dense K/V, D = 128), it uses fa_workspace_bytes() of scratch for the partial rows of units
+ * (D = 128), it uses fa_workspace_bytes() of scratch for the partial rows of units
  * cut between CTAs; with less scratch (or none) it runs one unit per CTA. */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
                  int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,

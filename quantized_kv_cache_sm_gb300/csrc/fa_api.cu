@@ -108,10 +108,9 @@ fa_status check_common(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_
 // decode scratch of one pair of cache formats (0 for Sq >= 2)
 size_t workspace_for(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
                      int causal, bool kq4, bool vq4, int* nsplit_out, int* chunk_out) {
-  if (Sq != 1)  // the cut schedule runs for dense K/V at D = 128
-    return (kq4 || vq4 || D != 128)
-               ? 0
-               : prefill_workspace_bytes(B, Hq, Sq, Sk, q_pos_offset, causal, D, num_sms());
+  if (Sq != 1)  // the prefill's cut schedule runs at D = 128
+    return D != 128 ? 0
+                    : prefill_workspace_bytes(B, Hq, Sq, Sk, q_pos_offset, causal, D, num_sms());
   const int sk_eff = causal ? q_pos_offset + 1 : Sk;
   int ns = 1, ck = sk_eff;
   decode_plan(B, Hkv, sk_eff, num_sms(), kq4, vq4, &ns, &ck);

@@ -847,7 +847,8 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
 // ------------------------------------------------------------------------------------------
 // The same kernel run over segments of work units (the equal-cuts schedule below): every role
 // walks this CTA's segments, a unit cut between CTAs is published as partial rows and merged by
-// its last piece.  Used where cutting beats one unit per CTA (more units than SMs, long units).
+// its last piece.  Used at D = 128 where cutting beats one unit per CTA (more units than SMs,
+// long units).
 // ------------------------------------------------------------------------------------------
 template <int D, bool BF16, bool KQ4, bool VQ4>
 __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
@@ -1450,18 +1451,19 @@ static cudaError_t launch_fmt(const PrefillLaunch& L, cudaStream_t stream) {
                : launch_t<D, BF16, false, false>(L, stream);
 }
 
-// equal cuts of the step sequence over one CTA per SM (dense K/V, D = 128)
-template <bool BF16>
+// equal cuts of the step sequence over one CTA per SM (D = 128, any pair of K/V formats)
+template <bool BF16, bool KQ4, bool VQ4>
 static cudaError_t launch_seg(const PrefillLaunch& L, const Plan& p, cudaStream_t stream) {
-  using C = Cfg<128, false, false>;
-  auto kern = prefill_seg_kernel<128, BF16, false, false>;
+  using C = Cfg<128, KQ4, VQ4>;
+  static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
+  auto kern = prefill_seg_kernel<128, BF16, KQ4, VQ4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   PrefillArgs a;
   a.o = L.o;
-  a.k_scale = nullptr;
-  a.v_scale = nullptr;
+  a.k_scale = static_cast<const uint8_t*>(L.k_scale);
+  a.v_scale = static_cast<const uint8_t*>(L.v_scale);
   a.rescale_count = L.rescale_count;
   a.B = L.B;
   a.Hq = L.Hq;
@@ -1483,11 +1485,19 @@ static cudaError_t launch_seg(const PrefillLaunch& L, const Plan& p, cudaStream_
   return cudaGetLastError();
 }
 
+template <bool BF16>
+static cudaError_t launch_seg_fmt(const PrefillLaunch& L, const Plan& p, cudaStream_t stream) {
+  if (L.kq4) return L.vq4 ? launch_seg<BF16, true, true>(L, p, stream)
+                          : launch_seg<BF16, true, false>(L, p, stream);
+  return L.vq4 ? launch_seg<BF16, false, true>(L, p, stream)
+               : launch_seg<BF16, false, false>(L, p, stream);
+}
+
 cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream) {
-  if (L.D == 128 && !L.kq4 && !L.vq4) {
+  if (L.D == 128) {
     const Plan p = make_plan(L.B, L.Hq, L.Sq, L.Sk, L.q_pos_offset, L.causal, L.D, L.num_sms);
     if (!p.whole && L.workspace != nullptr && L.workspace_bytes >= p.bytes)
-      return L.bf16 ? launch_seg<true>(L, p, stream) : launch_seg<false>(L, p, stream);
+      return L.bf16 ? launch_seg_fmt<true>(L, p, stream) : launch_seg_fmt<false>(L, p, stream);
   }
   if (L.D == 128)
     return L.bf16 ? launch_fmt<128, true>(L, stream) : launch_fmt<128, false>(L, stream);

@@ -136,3 +136,34 @@ def test_cut_schedule_other_shapes(fa, shape):
     check_close(np64(o_cut).reshape(-1, 128)[rows], want, dtype, f"{shape} cut schedule")
     diff = (o_cut.float() - o_whole.float()).abs().max().item()
     assert diff <= (4e-3 if dtype == "f16" else 3e-2), diff
+
+
+@pytest.mark.parametrize("fmt", [("q4_0", "q4_0"), ("dense", "q4_0"), ("q4_0", "dense")],
+                         ids=lambda f: f"{f[0]}K-{f[1]}V")
+def test_cut_schedule_q4_0_caches(fa, fmt):
+    """The cut schedule with q4_0 K and/or V: the dequant warps' tile stream runs on across
+    segments; compared with the oracle (its own quantization, dequantized exactly) on sampled
+    rows and with the one-unit-per-CTA launch."""
+    from gpu_common import oracle_q4_planes
+    w = fa_inputs.WORKLOADS["prefill_gqa32x8_d128_sq2048_sk16384_f16"]
+    q, k, v = fa_inputs.make_qkv(w)
+
+    def side(x, f):
+        if f == "q4_0":
+            nib, sc = oracle_q4_planes(x)
+            return fa.fa_quantize_q4_0(x.cuda()), oracle.dequantize_q4_0(nib, sc)
+        return x.cuda(), np64(x)
+
+    kd, k64 = side(k, fmt[0])
+    vd, v64 = side(v, fmt[1])
+    ws = workspace_for(fa, w)
+    qd = q.cuda()
+    o_cut = fa.fa_fwd_kv(qd, kd, vd, causal=True, q_pos_offset=w.q_pos_offset, workspace=ws)
+    o_whole = fa.fa_fwd_kv(qd, kd, vd, causal=True, q_pos_offset=w.q_pos_offset)
+    assert fa.fa_get_status() == fa.FA_OK
+    rows = sample_rows(w.B, w.Hq, w.Sq, per_head=8, seed=5)
+    want = oracle.attention(np64(q), k64, v64, causal=True, q_pos_offset=w.q_pos_offset,
+                            scale=w.scale, rows=rows)
+    check_close(np64(o_cut).reshape(-1, w.D)[rows], want, w.dtype, f"{fmt} cut schedule")
+    diff = (o_cut.float() - o_whole.float()).abs().max().item()
+    assert diff <= 4e-3, diff
