@@ -223,8 +223,9 @@ fa_status fa_append_q4_0(const void* k_new, const void* v_new, void* k_cache, vo
 /* Synchronize `stream`, then report (and clear) any device-side error recorded by this
  * library's kernels since the last call: FA_ERR_TIMEOUT when a bounded wait inside a kernel ran
  * out (the kernel then abandoned its work and returned), FA_ERR_INVALID_ARG when a device-side
- * index input was out of range (fa_decode_paged), FA_ERR_CUDA when the stream reports a CUDA
- * error, FA_OK otherwise. */
+ * index input was out of range (fa_decode_paged), FA_ERR_UNSUPPORTED when a prefill CTA's
+ * share of the work did not fit its segment table (see fa_prefill_schedule; the launch plans
+ * never produce one), FA_ERR_CUDA when the stream reports a CUDA error, FA_OK otherwise. */
 fa_status fa_get_status(fa_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */
@@ -236,8 +237,37 @@ const char* fa_status_string(fa_status s);
  * or hang is involved. */
 fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream);
 
+/* The prefill's work schedule for a call of this shape on a device with `num_sms` SMs, computed
+ * on the host by the same code the kernel runs (no device is needed or touched).  The schedule
+ * is this library's own arrangement of the sums that fa_fwd computes (attention forward, the
+ * sections cited at fa_fwd): it changes which CTA adds which key blocks, not the result's
+ * definition.
+ *
+ * A work unit is a pair of consecutive 128-row query tiles (A at q0A, B at q0A + 128) of one
+ * query head and batch; it takes nbmax = max(nbA, nbB) key-block steps, where nbA and nbB are the
+ * 128-key blocks holding any key visible to tile A or B.  Units are ordered by pair index from
+ * the last query tiles to the first, then batch, then head, and their steps concatenated into W
+ * steps.  When the plan cuts (D = 128, more units than SMs, and an estimate favours it), CTA c
+ * of num_sms runs the steps [floor(c W / num_sms), floor((c + 1) W / num_sms)).
+ *
+ * plan (5 values, may be NULL): {cut (1) or one unit per CTA (0), CTAs of the cut launch (0 when
+ * not cut), W, units, workspace bytes the cut needs}.  force_cut != 0 lays the cuts out over
+ * num_sms CTAs even where the plan keeps whole units (plan[0] still reports the plan's choice).
+ * rows (max_rows x 11 int64, row-major, caller-owned, may be NULL when max_rows is 0): one row
+ * per segment, CTA by CTA in order: {cta, batch, query head, q0A, nbA, nbB, nbmax, j0, j1,
+ * unit_start, slot} -- steps [j0, j1) of the unit whose step 0 is global step unit_start; slot is
+ * the partial-result slot (0 or 1) of a unit cut between CTAs, else -1.
+ * Returns the number of segments (rows beyond max_rows are counted, not written), 0 when the
+ * launch runs one unit per CTA, -1 when a CTA's range needs more segments than the kernel's
+ * segment table holds (only under force_cut: the plan keeps whole units for such shapes; a
+ * kernel that met it would stop and fa_get_status would report FA_ERR_UNSUPPORTED), -2 for
+ * invalid arguments (the checks of fa_fwd; Sq >= 2; num_sms >= 1). */
+int64_t fa_prefill_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
+                            int causal, int num_sms, int force_cut, int64_t* plan,
+                            int64_t* rows, int64_t max_rows);
+
 /* Library ABI version (major * 100 + minor): 101 adds fa_fwd_kv and fa_append_q4_0, 102
- * fa_decode_paged, 103 fa_fwd_explicit. */
+ * fa_decode_paged, 103 fa_fwd_explicit, 104 fa_prefill_schedule. */
 int fa_version(void);
 
 #ifdef __cplusplus

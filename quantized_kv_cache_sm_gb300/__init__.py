@@ -27,6 +27,7 @@ EXPORTED = (
     "fa_quantize_q4_0", "fa_get_status", "fa_status_string", "fa_debug_wait_timeout",
     "fa_version", "fa_fwd_decode_noalloc", "fa_fwd_kv", "fa_append_q4_0", "fa_decode_paged",
     "fa_decode_paged_workspace_bytes", "fa_fwd_explicit", "fa_explicit_workspace_bytes",
+    "fa_prefill_schedule",
 )
 
 _lib = None
@@ -78,6 +79,8 @@ def load_from(p: str) -> ctypes.CDLL:
     lib.fa_debug_wait_timeout.restype = i
     lib.fa_version.argtypes = []
     lib.fa_version.restype = i
+    lib.fa_prefill_schedule.argtypes = [i] * 10 + [vp, vp, ctypes.c_int64]
+    lib.fa_prefill_schedule.restype = ctypes.c_int64
     lib.fa_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_decode_noalloc.restype = i
     lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, i, vp, sz, vp,
@@ -260,6 +263,36 @@ def fa_debug_wait_timeout(limit_ns: int, stream=None) -> None:
 
 def fa_version() -> int:
     return int(load().fa_version())
+
+
+SCHEDULE_COLUMNS = ("cta", "b", "h", "q0A", "nbA", "nbB", "nbmax", "j0", "j1", "unit_start",
+                    "slot")
+
+
+def fa_prefill_schedule(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, num_sms, *,
+                        force_cut: bool = False):
+    """The prefill's work schedule for a call of this shape on `num_sms` SMs, as the kernel
+    computes it (host only).  Returns (plan, rows): plan = dict(cut, ctas, W, units,
+    workspace_bytes); rows = int64 array [segments, 11] with columns SCHEDULE_COLUMNS, empty when
+    the launch runs one unit per CTA.  Raises FaError(FA_ERR_INVALID_ARG) for invalid arguments
+    and FaError(FA_ERR_UNSUPPORTED) when a CTA's range does not fit the segment table."""
+    import numpy as np
+    lib = load()
+    plan = (ctypes.c_int64 * 5)()
+    args = [int(B), int(Hq), int(Hkv), int(Sq), int(Sk), int(D), int(q_pos_offset),
+            int(bool(causal)), int(num_sms), int(bool(force_cut))]
+    n = lib.fa_prefill_schedule(*args, plan, None, 0)
+    if n == -2:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_prefill_schedule")
+    if n == -1:
+        raise FaError(FA_ERR_UNSUPPORTED, "fa_prefill_schedule")
+    rows = np.zeros((n, len(SCHEDULE_COLUMNS)), dtype=np.int64)
+    if n > 0:
+        got = lib.fa_prefill_schedule(*args, plan, rows.ctypes.data, n)
+        assert got == n
+    info = dict(zip(("cut", "ctas", "W", "units", "workspace_bytes"), (int(x) for x in plan)))
+    info["cut"] = bool(info["cut"])
+    return info, rows
 
 
 def fa_fwd_decode_noalloc(q, k, v, o=None, *, causal: bool = True,

@@ -474,6 +474,7 @@ fa_status fa_get_status(fa_stream_t stream) {
     return FA_ERR_CUDA;
   if (a == 0xffffffffu || b == 0xffffffffu) return FA_ERR_CUDA;
   if (b == kErrBadIndex) return FA_ERR_INVALID_ARG;
+  if (a == kErrSchedule) return FA_ERR_UNSUPPORTED;
   if (a || b || c) return FA_ERR_TIMEOUT;
   return FA_OK;
 }
@@ -497,6 +498,17 @@ fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream) {
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_version(void) { return 103; }
+int64_t fa_prefill_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
+                            int causal, int num_sms, int force_cut, int64_t* plan, int64_t* rows,
+                            int64_t max_rows) {
+  if (Sq < 2 || num_sms < 1 || max_rows < 0 || (max_rows > 0 && rows == nullptr) ||
+      check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, 1.f, FA_F16, FA_KV_DENSE) !=
+          FA_OK)
+    return -2;
+  return prefill_debug_schedule(B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, D, num_sms,
+                                force_cut != 0, plan, rows, max_rows);
+}
+
+int fa_version(void) { return 104; }
 
 }  // extern "C"

@@ -28,6 +28,14 @@ cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream);
 size_t prefill_workspace_bytes(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causal,
                                int D, int num_sms);
 uint32_t prefill_take_error();
+// the cut schedule of a prefill call of this shape on num_sms SMs, computed on the host by the
+// kernel's own segment code: the plan {cut, CTAs, steps W, units, workspace bytes} and one row
+// of kScheduleRowWidth values per segment; returns the segment count, -1 if a CTA's range does
+// not fit its segment table.  force_cut lays out the cuts even where the plan keeps whole units.
+constexpr int kScheduleRowWidth = 11;
+int64_t prefill_debug_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int q_pos_offset,
+                               int causal, int D, int num_sms, bool force_cut, int64_t* plan,
+                               int64_t* rows, int64_t max_rows);
 
 struct DecodeLaunch {
   CUtensorMap tm_k, tm_v;        // K/V tiles (dense) or nibble tiles (q4_0)

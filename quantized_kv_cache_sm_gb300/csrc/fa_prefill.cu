@@ -218,7 +218,7 @@ __device__ __forceinline__ float block_row_exp(uint32_t scol, int rel_lim, float
 }
 
 // number of 128-key blocks a query tile starting at row q0 must visit
-__device__ __forceinline__ int tile_blocks(const PrefillArgs& a, int q0) {
+__host__ __device__ __forceinline__ int tile_blocks(const PrefillArgs& a, int q0) {
   if (q0 >= a.Sq) return 0;
   const int last_row = min(q0 + kBM - 1, a.Sq - 1);
   const int kend = a.causal ? min(a.Sk, a.q_pos_offset + last_row + 1) : a.Sk;
@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
 // steps and none idles through a last partial wave.  A unit cut between CTAs is finished by
 // whichever of its CTAs finds all its pieces published.
 // ------------------------------------------------------------------------------------------
-__device__ __forceinline__ int pair_steps(const PrefillArgs& a, int z) {
+__host__ __device__ __forceinline__ int pair_steps(const PrefillArgs& a, int z) {
   const int q0A = 2 * (a.n_pairs - 1 - z) * kBM;
   return max(tile_blocks(a, q0A), tile_blocks(a, q0A + kBM));
 }
@@ -656,7 +656,8 @@ struct SegS {
 
 // the segment that starts at global step t of a range ending at t_end; false if t lies past
 // the last unit, which a consistent schedule never asks for
-__device__ __forceinline__ bool locate(const PrefillArgs& a, int64_t t, int64_t t_end, Seg& sg) {
+__host__ __device__ __forceinline__ bool locate(const PrefillArgs& a, int64_t t, int64_t t_end,
+                                                Seg& sg) {
   const int64_t per_class = static_cast<int64_t>(a.B) * a.Hq;
   int64_t acc = 0;
   int z = 0;
@@ -684,23 +685,37 @@ __device__ __forceinline__ bool locate(const PrefillArgs& a, int64_t t, int64_t 
   return sg.j1 > sg.j0;
 }
 // first global step of CTA c's range (equal cuts)
-__device__ __forceinline__ int64_t range_start(const PrefillArgs& a, int c) {
+__host__ __device__ __forceinline__ int64_t range_start(const PrefillArgs& a, int c) {
   return c >= a.n_ctas ? a.W : static_cast<int64_t>(c) * a.W / a.n_ctas;
 }
 // the CTA whose range holds global step t
-__device__ __forceinline__ int cta_of(const PrefillArgs& a, int64_t t) {
+__host__ __device__ __forceinline__ int cta_of(const PrefillArgs& a, int64_t t) {
   return static_cast<int>(((t + 1) * a.n_ctas - 1) / a.W);
 }
 // the same, and a piece's partial slot, on plain scalars (W steps over n CTAs): slot 0 when the
 // unit is where CTA c's range begins, 1 when the CTA reached it after other segments
-__device__ __forceinline__ int64_t cut_start(int c, int64_t W, int n) {
+__host__ __device__ __forceinline__ int64_t cut_start(int c, int64_t W, int n) {
   return c >= n ? W : static_cast<int64_t>(c) * W / n;
 }
-__device__ __forceinline__ int cut_cta_of(int64_t t, int64_t W, int n) {
+__host__ __device__ __forceinline__ int cut_cta_of(int64_t t, int64_t W, int n) {
   return static_cast<int>(((t + 1) * n - 1) / W);
 }
-__device__ __forceinline__ int cut_slot(int c, int64_t unit_start, int64_t W, int n) {
+__host__ __device__ __forceinline__ int cut_slot(int c, int64_t unit_start, int64_t W, int n) {
   return cut_start(c, W, n) >= unit_start ? 0 : 1;
+}
+// CTA c's segments in order (at most kMaxSegs); -1 if its range does not fit the table or
+// runs past the last unit, which a consistent plan never produces
+__host__ __device__ __forceinline__ int build_segments(const PrefillArgs& a, int c, SegS* segs) {
+  const int64_t t_end = range_start(a, c + 1);
+  int ns = 0;
+  for (int64_t tt = range_start(a, c); tt < t_end;) {
+    Seg sg;
+    if (ns >= kMaxSegs || !locate(a, tt, t_end, sg)) return -1;
+    segs[ns] = SegS{sg.b, sg.h, sg.q0A, sg.nbA, sg.nbB, sg.nbmax, sg.j0, sg.j1, sg.unit_start};
+    ++ns;
+    tt += sg.j1 - sg.j0;
+  }
+  return ns;
 }
 // one tile of a piece, column-major so that a warp's 32 rows of one column are 128 contiguous
 // bytes: [D + 4 columns][128 rows] f32, columns O[0..D), frame, row sum, frame moves, pad
@@ -903,17 +918,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     // this CTA's segments, once: the roles read them back instead of each locating them
-    int ns = 0;
-    for (int64_t tt = t_begin; tt < t_end;) {
-      Seg sg;
-      if (ns >= kMaxSegs || !locate(args, tt, t_end, sg)) {
-        schedule_fault(abort_flag);
-        ns = 0;
-        break;
-      }
-      segs[ns] = SegS{sg.b, sg.h, sg.q0A, sg.nbA, sg.nbB, sg.nbmax, sg.j0, sg.j1, sg.unit_start};
-      ++ns;
-      tt += sg.j1 - sg.j0;
+    int ns = build_segments(args, cta, segs);
+    if (ns < 0) {
+      schedule_fault(abort_flag);
+      ns = 0;
     }
     *seg_count = ns;
   }
@@ -1359,35 +1367,40 @@ struct Plan {
   bool whole;
   size_t flag_bytes, bytes;
 };
+// the fields of PrefillArgs that the cut schedule reads, for a call of this shape
+static PrefillArgs schedule_args(int B, int Hq, int Hkv, int Sq, int Sk, int q_pos_offset,
+                                 int causal) {
+  PrefillArgs a{};
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.Scap = Sk;
+  a.q_pos_offset = causal ? q_pos_offset : 0;
+  a.causal = causal;
+  a.n_qtiles = (Sq + kBM - 1) / kBM;
+  a.n_pairs = (a.n_qtiles + 1) / 2;
+  return a;
+}
+
 static Plan make_plan(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causal, int D,
                       int num_sms) {
-  auto blocks = [&](int q0) -> int64_t {  // the device's tile_blocks, on the host
-    if (q0 >= Sq) return 0;
-    const int last_row = q0 + kBM - 1 < Sq - 1 ? q0 + kBM - 1 : Sq - 1;
-    const int64_t kend = causal ? (Sk < static_cast<int64_t>(q_pos_offset) + last_row + 1
-                                       ? Sk
-                                       : static_cast<int64_t>(q_pos_offset) + last_row + 1)
-                                : Sk;
-    return (kend + kBN - 1) / kBN;
-  };
-  const int n_qtiles = (Sq + kBM - 1) / kBM;
-  const int n_pairs = (n_qtiles + 1) / 2;
+  const PrefillArgs a = schedule_args(B, Hq, Hq, Sq, Sk, q_pos_offset, causal);
   const int64_t per_class = static_cast<int64_t>(B) * Hq;
   Plan p;
-  p.units = per_class * n_pairs;
+  p.units = per_class * a.n_pairs;
   p.W = 0;
   int64_t nb_min = 0;  // the shortest unit
-  for (int z = 0; z < n_pairs; ++z) {
-    const int q0A = 2 * (n_pairs - 1 - z) * kBM;
-    const int64_t a = blocks(q0A), b = blocks(q0A + kBM);
-    const int64_t nb = a > b ? a : b;
+  for (int z = 0; z < a.n_pairs; ++z) {
+    const int64_t nb = pair_steps(a, z);
     p.W += per_class * nb;
     if (z == 0 || nb < nb_min) nb_min = nb;
   }
   // a CTA's range spans at most ceil(steps / nb_min) + 2 segments, which must fit its table
   const int64_t per_cta = num_sms > 0 ? (p.W + num_sms - 1) / num_sms : 0;
   const bool fits = nb_min > 0 && (per_cta + nb_min - 1) / nb_min + 2 <= kMaxSegs;
-  bool cuts = num_sms > 0 && p.units > num_sms && fits;
+  bool cuts = D == 128 && num_sms > 0 && p.units > num_sms && fits;
   if (cuts) {
     const double avg = static_cast<double>(p.W) / static_cast<double>(p.units);
     const double whole_est = static_cast<double>((p.units + num_sms - 1) / num_sms) * avg;
@@ -1407,6 +1420,48 @@ static Plan make_plan(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causa
 size_t prefill_workspace_bytes(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causal,
                                int D, int num_sms) {
   return make_plan(B, Hq, Sq, Sk, causal ? q_pos_offset : 0, causal, D, num_sms).bytes;
+}
+
+int64_t prefill_debug_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int q_pos_offset,
+                               int causal, int D, int num_sms, bool force_cut, int64_t* plan,
+                               int64_t* rows, int64_t max_rows) {
+  const Plan p = make_plan(B, Hq, Sq, Sk, q_pos_offset, causal, D, num_sms);
+  PrefillArgs a = schedule_args(B, Hq, Hkv, Sq, Sk, q_pos_offset, causal);
+  const bool cut = !p.whole || (force_cut && num_sms > 0 && p.W > 0);
+  a.W = p.W;
+  a.n_ctas = cut ? num_sms : 0;
+  if (plan != nullptr) {
+    plan[0] = p.whole ? 0 : 1;
+    plan[1] = a.n_ctas;
+    plan[2] = p.W;
+    plan[3] = p.units;
+    plan[4] = static_cast<int64_t>(p.bytes);
+  }
+  if (!cut) return 0;
+  int64_t n = 0;
+  SegS segs[kMaxSegs];
+  for (int c = 0; c < a.n_ctas; ++c) {
+    const int ns = build_segments(a, c, segs);
+    if (ns < 0) return -1;
+    for (int i = 0; i < ns; ++i, ++n) {
+      if (rows == nullptr || n >= max_rows) continue;
+      const SegS& g = segs[i];
+      const bool split = cta_of(a, g.unit_start) != cta_of(a, g.unit_start + g.nbmax - 1);
+      int64_t* r = rows + n * kScheduleRowWidth;
+      r[0] = c;
+      r[1] = g.b;
+      r[2] = g.h;
+      r[3] = g.q0A;
+      r[4] = g.nbA;
+      r[5] = g.nbB;
+      r[6] = g.nbmax;
+      r[7] = g.j0;
+      r[8] = g.j1;
+      r[9] = g.unit_start;
+      r[10] = split ? cut_slot(c, g.unit_start, a.W, a.n_ctas) : -1;
+    }
+  }
+  return n;
 }
 
 template <int D, bool BF16, bool KQ4, bool VQ4>
