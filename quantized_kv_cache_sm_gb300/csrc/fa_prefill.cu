@@ -217,6 +217,131 @@ __device__ __forceinline__ float block_row_exp(uint32_t scol, int rel_lim, float
   return la + lb;
 }
 
+// Single-read form of the two passes above: the row's 128 scores of S(j) read from TMEM with
+// one wait (keys past rel_lim set to -inf when MASK) and kept in registers for the
+// exponentials.  Same values, same summation order.
+template <bool MASK>
+__device__ __forceinline__ float block_row_load(uint32_t scol, int rel_lim, float (&s)[kBN]) {
+  uint32_t r0[32], r1[32], r2[32], r3[32];
+  tmem_ld32(scol, r0);
+  tmem_ld32(scol + 32, r1);
+  tmem_ld32(scol + 64, r2);
+  tmem_ld32(scol + 96, r3);
+  tmem_wait_ld();
+  reg_fence32(r0);
+  reg_fence32(r1);
+  reg_fence32(r2);
+  reg_fence32(r3);
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    s[i] = __uint_as_float(r0[i]);
+    s[32 + i] = __uint_as_float(r1[i]);
+    s[64 + i] = __uint_as_float(r2[i]);
+    s[96 + i] = __uint_as_float(r3[i]);
+    if (MASK) {
+      if (i > rel_lim) s[i] = -INFINITY;
+      if (32 + i > rel_lim) s[32 + i] = -INFINITY;
+      if (64 + i > rel_lim) s[64 + i] = -INFINITY;
+      if (96 + i > rel_lim) s[96 + i] = -INFINITY;
+    }
+    m0 = fmaxf(m0, s[i]);
+    m1 = fmaxf(m1, s[32 + i]);
+    m2 = fmaxf(m2, s[64 + i]);
+    m3 = fmaxf(m3, s[96 + i]);
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+template <bool BF16>
+__device__ __forceinline__ float block_row_exp_regs(uint32_t scol, const float (&s)[kBN],
+                                                    float sl2, float nf) {
+  float la = 0.f, lb = 0.f;
+#pragma unroll
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t pr[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float p0 = ex2(fmaf(s[32 * c + 2 * i], sl2, nf));
+      const float p1 = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, nf));
+      if (i & 1) lb += p0 + p1; else la += p0 + p1;
+      pr[i] = pack2<BF16>(p0, p1);
+    }
+    tmem_st16(scol + 16 * c, pr);
+  }
+  return la + lb;
+}
+
+// One key block of the online softmax for this thread's query row: read S(j), move the frame f
+// to the block max when that exceeds f by more than the margin (l and, when it already holds
+// earlier blocks (o_live), O are scaled by 2^(f_old - f)), write P = 2^(s - f) over S and add
+// its row sum to l.  O may be rescaled in place: S(j) being ready means PV(j-1) has completed
+// (QK(j) was issued after it).  The caller waits for the TMEM stores.
+//
+// ONE_READ selects the single-read form (one TMEM wait per block, 128 scores in registers)
+// over the two-pass form (six waits, fewer live registers).  Measured per kernel: the single
+// read is faster in the one-unit-per-CTA kernel and in the cut-schedule kernel with exactly
+// one q4_0 side (by 11 % with a q4_0 V), slower by 2 % in the dense cut-schedule kernel, even
+// with q4_0 on both sides.
+template <int D, bool BF16, bool ONE_READ>
+__device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool need_mask,
+                                              int rel_lim, float sl2, bool o_live, float& f,
+                                              float& l, int& nres) {
+  auto rescale_o = [&](float alpha) {
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(ocol + 32 * c, r);
+      tmem_wait_ld();
+      reg_fence32(r);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+      tmem_st32(ocol + 32 * c, r);
+    }
+  };
+  if constexpr (ONE_READ) {
+    float s[kBN];
+    float mx;
+    if (need_mask)
+      mx = block_row_load<true>(scol, rel_lim, s);
+    else
+      mx = block_row_load<false>(scol, rel_lim, s);
+    const float m2 = mx * sl2;
+    const bool need = m2 > f + kMarginLog2;
+    const bool any = __any_sync(0xffffffffu, need);
+    float alpha = 1.f;
+    if (need) {
+      alpha = ex2(f - m2);
+      l *= alpha;
+      f = m2;
+      ++nres;
+    }
+    l += block_row_exp_regs<BF16>(scol, s, sl2, -f);
+    if (any && o_live) rescale_o(alpha);
+  } else {
+    // pass 1: row max over the 128 scores
+    const float mx = need_mask ? block_row_max<true>(scol, rel_lim)
+                               : block_row_max<false>(scol, rel_lim);
+    const float m2 = mx * sl2;
+    const bool need = m2 > f + kMarginLog2;
+    if (__any_sync(0xffffffffu, need)) {
+      const float alpha = need ? ex2(f - m2) : 1.f;
+      if (need) {
+        l *= alpha;
+        f = m2;
+        ++nres;
+      }
+      if (o_live) {
+        rescale_o(alpha);
+        tmem_wait_st();
+      }
+    }
+    // pass 2: P = 2^(t - f) over the first half of S, row sum
+    const float nf = -f;
+    l += need_mask ? block_row_exp<true, BF16>(scol, rel_lim, sl2, nf)
+                   : block_row_exp<false, BF16>(scol, rel_lim, sl2, nf);
+  }
+}
+
 // number of 128-key blocks a query tile starting at row q0 must visit
 __host__ __device__ __forceinline__ int tile_blocks(const PrefillArgs& a, int q0) {
   if (q0 >= a.Sq) return 0;
@@ -479,38 +604,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
       // last visible key of this row, relative to the block
       const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
-      // pass 1: row max over the 128 scores
-      const float mx = need_mask ? block_row_max<true>(scol, rel_lim)
-                                 : block_row_max<false>(scol, rel_lim);
-      const float m2 = mx * sl2;
-      const bool need = m2 > f + kMarginLog2;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ex2(f - m2) : 1.f;
-        if (need) {
-          l *= alpha;
-          f = m2;
-          ++nres;
-        }
-        // S(j) being ready means PV(j-1) has completed (QK(j) was issued after it), so O can be
-        // rescaled in place without a further wait
-        if (j > 0) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(ocol + 32 * c, r);
-            tmem_wait_ld();
-            reg_fence32(r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(ocol + 32 * c, r);
-          }
-          tmem_wait_st();
-        }
-      }
-      // pass 2: P = 2^(t - f) over the first half of S, row sum
-      const float nf = -f;
-      l += need_mask ? block_row_exp<true, BF16>(scol, rel_lim, sl2, nf)
-                     : block_row_exp<false, BF16>(scol, rel_lim, sl2, nf);
+      softmax_block<D, BF16, true>(scol, ocol, need_mask, rel_lim, sl2, j > 0, f, l, nres);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPReady + t));
@@ -1180,38 +1274,9 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
             (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
         // last visible key of this row, relative to the block
         const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
-        // pass 1: row max over the 128 scores
-        const float mx = need_mask ? block_row_max<true>(scol, rel_lim)
-                                   : block_row_max<false>(scol, rel_lim);
-        const float m2 = mx * sl2;
-        const bool need = m2 > f + kMarginLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2(f - m2) : 1.f;
-          if (need) {
-            l *= alpha;
-            f = m2;
-            ++nres;
-          }
-          // S(j) being ready means PV(j-1) has completed (QK(j) was issued after it), so O can be
-          // rescaled in place without a further wait (j > j0: O holds this segment's blocks)
-          if (j > j0) {
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(ocol + 32 * c, r);
-              tmem_wait_ld();
-              reg_fence32(r);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(ocol + 32 * c, r);
-            }
-            tmem_wait_st();
-          }
-        }
-        // pass 2: P = 2^(t - f) over the first half of S, row sum
-        const float nf = -f;
-        l += need_mask ? block_row_exp<true, BF16>(scol, rel_lim, sl2, nf)
-                       : block_row_exp<false, BF16>(scol, rel_lim, sl2, nf);
+        // O holds this segment's earlier blocks when j > j0
+        softmax_block<D, BF16, KQ4 != VQ4>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f, l,
+                                           nres);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarPReady + t));
