@@ -105,7 +105,8 @@ fa_status check_common(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_
   return FA_OK;
 }
 
-// decode scratch of one pair of cache formats (0 for Sq >= 2)
+// scratch of one call: the decode splits' flags and partials for one pair of cache formats, or
+// (Sq >= 2) the prefill cut schedule's flags and partial rows (0 when it runs whole units)
 size_t workspace_for(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_offset,
                      int causal, bool kq4, bool vq4, int* nsplit_out, int* chunk_out) {
   if (Sq != 1)  // the prefill's cut schedule runs at D = 128
