@@ -266,8 +266,29 @@ int64_t fa_prefill_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q
                             int causal, int num_sms, int force_cut, int64_t* plan,
                             int64_t* rows, int64_t max_rows);
 
+/* The decode kernels' work split, computed on the host by the kernels' own plan code (no device
+ * is needed or touched).  Like fa_prefill_schedule this is this library's arrangement of the
+ * decode sums (fa_fwd with Sq == 1, and fa_decode_paged): which CTA adds which keys, and the
+ * splits that the launch merges.
+ *  seq_lens == NULL: a uniform batch of B sequences of Sk keys each (fa_fwd decode at position
+ *    Sk - 1): every (sequence, kv head) is cut into the same number of splits of whole tiles;
+ *    one row per (sequence, split), B x splits rows.
+ *  seq_lens != NULL (host array of B lengths): a paged batch (fa_decode_paged) whose pages hold
+ *    page_size tokens, pages_per_seq per sequence; the CTAs of a kv head (the row count) are
+ *    shared out over the sequences in proportion to their lengths, at least one each, every
+ *    length clamped to [1, page_size * pages_per_seq] as the kernel does (which also reports
+ *    the out-of-range length); one row per CTA.  Sk is ignored.
+ * rows (max_rows x 5 int32, row-major, caller-owned; may be NULL when max_rows is 0):
+ * {sequence (-1: the CTA has no work), split, splits of that sequence, first key, end key}.
+ * Returns the number of rows (rows beyond max_rows are counted, not written), or -2 for
+ * invalid arguments (B, Hkv, num_sms >= 1; formats; Sk >= 1 when uniform; page_size >= 1 and
+ * a multiple of the kernel's tile, pages_per_seq >= 1, when paged). */
+int64_t fa_decode_schedule(const int32_t* seq_lens, int B, int Hkv, int Sk, int page_size,
+                           int pages_per_seq, fa_kv_format k_format, fa_kv_format v_format,
+                           int num_sms, int32_t* rows, int64_t max_rows);
+
 /* Library ABI version (major * 100 + minor): 101 adds fa_fwd_kv and fa_append_q4_0, 102
- * fa_decode_paged, 103 fa_fwd_explicit, 104 fa_prefill_schedule. */
+ * fa_decode_paged, 103 fa_fwd_explicit, 104 fa_prefill_schedule, 105 fa_decode_schedule. */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -27,7 +27,7 @@ EXPORTED = (
     "fa_quantize_q4_0", "fa_get_status", "fa_status_string", "fa_debug_wait_timeout",
     "fa_version", "fa_fwd_decode_noalloc", "fa_fwd_kv", "fa_append_q4_0", "fa_decode_paged",
     "fa_decode_paged_workspace_bytes", "fa_fwd_explicit", "fa_explicit_workspace_bytes",
-    "fa_prefill_schedule",
+    "fa_prefill_schedule", "fa_decode_schedule",
 )
 
 _lib = None
@@ -81,6 +81,8 @@ def load_from(p: str) -> ctypes.CDLL:
     lib.fa_version.restype = i
     lib.fa_prefill_schedule.argtypes = [i] * 10 + [vp, vp, ctypes.c_int64]
     lib.fa_prefill_schedule.restype = ctypes.c_int64
+    lib.fa_decode_schedule.argtypes = [vp] + [i] * 8 + [vp, ctypes.c_int64]
+    lib.fa_decode_schedule.restype = ctypes.c_int64
     lib.fa_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_decode_noalloc.restype = i
     lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, i, vp, sz, vp,
@@ -293,6 +295,34 @@ def fa_prefill_schedule(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, num_sms, *,
     info = dict(zip(("cut", "ctas", "W", "units", "workspace_bytes"), (int(x) for x in plan)))
     info["cut"] = bool(info["cut"])
     return info, rows
+
+
+def fa_decode_schedule(B, Hkv, num_sms, *, Sk: int | None = None, seq_lens=None,
+                       page_size: int = 0, pages_per_seq: int = 0, k_format: str = "q4_0",
+                       v_format: str = "q4_0"):
+    """The decode kernels' work split (host only): an int32 array [rows, 5] of (sequence, split,
+    splits of that sequence, first key, end key).  Uniform batch: give Sk (one row per sequence
+    and split).  Paged batch: give seq_lens (B lengths), page_size and pages_per_seq (one row per
+    CTA of a kv head; sequence -1 for a CTA with no work).  Raises FaError(FA_ERR_INVALID_ARG)
+    for invalid arguments."""
+    import numpy as np
+    lib = load()
+    fmt = {"dense": FA_KV_DENSE, "q4_0": FA_KV_Q4_0}
+    lens = None
+    if seq_lens is not None:
+        lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+        if lens.shape != (int(B),):
+            raise ValueError("seq_lens must hold B lengths")
+    args = [lens.ctypes.data if lens is not None else None, int(B), int(Hkv),
+            int(Sk or 0), int(page_size), int(pages_per_seq), fmt[k_format], fmt[v_format],
+            int(num_sms)]
+    n = lib.fa_decode_schedule(*args, None, 0)
+    if n < 0:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_decode_schedule")
+    rows = np.zeros((n, 5), dtype=np.int32)
+    if n > 0:
+        assert lib.fa_decode_schedule(*args, rows.ctypes.data, n) == n
+    return rows
 
 
 def fa_fwd_decode_noalloc(q, k, v, o=None, *, causal: bool = True,

@@ -510,6 +510,28 @@ int64_t fa_prefill_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q
                                 force_cut != 0, plan, rows, max_rows);
 }
 
-int fa_version(void) { return 104; }
+int64_t fa_decode_schedule(const int32_t* seq_lens, int B, int Hkv, int Sk, int page_size,
+                           int pages_per_seq, fa_kv_format k_format, fa_kv_format v_format,
+                           int num_sms, int32_t* rows, int64_t max_rows) {
+  if (B < 1 || Hkv < 1 || num_sms < 1 || max_rows < 0 || (max_rows > 0 && rows == nullptr))
+    return -2;
+  if ((k_format != FA_KV_DENSE && k_format != FA_KV_Q4_0) ||
+      (v_format != FA_KV_DENSE && v_format != FA_KV_Q4_0))
+    return -2;
+  const bool kq4 = k_format == FA_KV_Q4_0, vq4 = v_format == FA_KV_Q4_0;
+  int cap = 0;
+  if (seq_lens == nullptr) {
+    if (Sk < 1) return -2;
+  } else {
+    if (page_size < 1 || pages_per_seq < 1 || page_size % decode_tile_keys(kq4, vq4) != 0)
+      return -2;
+    const int64_t c = static_cast<int64_t>(page_size) * pages_per_seq;
+    if (c > (1 << 30)) return -2;
+    cap = static_cast<int>(c);
+  }
+  return decode_debug_schedule(seq_lens, B, Hkv, Sk, cap, kq4, vq4, num_sms, rows, max_rows);
+}
+
+int fa_version(void) { return 105; }
 
 }  // extern "C"

@@ -200,6 +200,46 @@ struct DecodeArgs {
   int B;
 };
 
+// Paged batch: the `nsplit` CTAs of a kv head are shared out over the B sequences in proportion
+// to their lengths in tiles of `tile_keys` keys, at least one CTA each; every CTA computes the
+// same plan from the lengths.  A sequence's length is clamped to [1, cap] here (an out-of-range
+// length is reported by the kernel).  For CTA `cta`: its sequence b, its split within the
+// sequence, the sequence's split count and the index of its first CTA; false when the CTA lies
+// past the plan.  Runs on the host too (seq_lens then in host memory).
+struct PagedSlot {
+  int b, split, nsplit_b, first;
+};
+__host__ __device__ __forceinline__ int paged_len(const int32_t* seq_lens, int b, int cap) {
+  const int n = seq_lens[b];
+  return max(1, min(n, cap));
+}
+__host__ __device__ __forceinline__ bool paged_slot(const int32_t* seq_lens, int B, int cap,
+                                                    int nsplit, int tile_keys, int cta,
+                                                    PagedSlot& ps) {
+  int64_t total = 0;  // tiles of the whole batch
+  for (int bb = 0; bb < B; ++bb) total += (paged_len(seq_lens, bb, cap) + tile_keys - 1) / tile_keys;
+  const int spare = nsplit - B;  // CTAs beyond one per sequence
+  int s = cta;
+  for (int bb = 0; bb < B; ++bb) {
+    const int t = (paged_len(seq_lens, bb, cap) + tile_keys - 1) / tile_keys;
+    const int ns = 1 + static_cast<int>(static_cast<int64_t>(spare) * t / total);
+    if (s < ns) {
+      ps.b = bb;
+      ps.split = s;
+      ps.nsplit_b = ns;
+      ps.first = cta - s;
+      return true;
+    }
+    s -= ns;
+  }
+  return false;
+}
+// keys per split of a sequence of `len` keys cut into `nsplit_b` splits of whole tiles
+__host__ __device__ __forceinline__ int paged_chunk(int len, int nsplit_b, int tile_keys) {
+  const int tiles = (len + tile_keys - 1) / tile_keys;
+  return (tiles + nsplit_b - 1) / nsplit_b * tile_keys;
+}
+
 template <int D, bool BF16, bool KQ4, bool VQ4, bool PAGED>
 __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -229,36 +269,21 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
   int first = 0;  // paged: the plan index of this sequence's first CTA
   if constexpr (PAGED) {
     const int cap = args.pages_per_seq * args.page_size;
-    auto len_of = [&](int bb) {
-      const int n = args.seq_lens[bb];
-      return max(1, min(n, cap));
-    };
-    int64_t total = 0;  // tiles of the whole batch
-    for (int bb = 0; bb < args.B; ++bb) total += (len_of(bb) + kTileKeys - 1) / kTileKeys;
-    const int spare = args.nsplit - args.B;  // CTAs beyond one per sequence
-    int s = blockIdx.x;
-    b = -1;
-    for (int bb = 0; bb < args.B; ++bb) {
-      const int t = (len_of(bb) + kTileKeys - 1) / kTileKeys;
-      const int ns = 1 + static_cast<int>(static_cast<int64_t>(spare) * t / total);
-      if (s < ns) {
-        b = bb;
-        split = s;
-        nsplit_b = ns;
-        first = static_cast<int>(blockIdx.x) - s;
-        break;
-      }
-      s -= ns;
-    }
-    if (b < 0) return;  // nothing planned for this CTA (no barrier or memory touched yet)
+    PagedSlot ps;
+    if (!paged_slot(args.seq_lens, args.B, cap, args.nsplit, kTileKeys,
+                    static_cast<int>(blockIdx.x), ps))
+      return;  // nothing planned for this CTA (no barrier or memory touched yet)
+    b = ps.b;
+    split = ps.split;
+    nsplit_b = ps.nsplit_b;
+    first = ps.first;
     sk_b = args.seq_lens[b];
     if (sk_b < 1 || sk_b > cap) {
       if (threadIdx.x == 0 && split == 0 && hkv == 0)
         atomicCAS(&g_decode_error, kErrNone, kErrBadIndex);
       sk_b = max(1, min(sk_b, cap));
     }
-    const int tiles = (sk_b + kTileKeys - 1) / kTileKeys;
-    chunk = (tiles + nsplit_b - 1) / nsplit_b * kTileKeys;
+    chunk = paged_chunk(sk_b, nsplit_b, kTileKeys);
   }
   // slots of the partials and flags.  Uniform batch: [B, Hq, nsplit] partial rows, [B, Hkv,
   // nsplit] flags.  Paged batch: one slot per (kv head, plan CTA): [Hkv, nsplit, G] partial rows,
@@ -972,6 +997,47 @@ cudaError_t decode_launch(const DecodeLaunch& L, cudaStream_t stream) {
   if (L.D == 128)
     return L.bf16 ? launch_fmt<128, true>(L, stream) : launch_fmt<128, false>(L, stream);
   return L.bf16 ? launch_fmt<64, true>(L, stream) : launch_fmt<64, false>(L, stream);
+}
+
+int64_t decode_debug_schedule(const int32_t* seq_lens, int B, int Hkv, int Sk, int cap,
+                              bool kq4, bool vq4, int num_sms, int32_t* rows,
+                              int64_t max_rows) {
+  const int tile = decode_tile_keys(kq4, vq4);
+  int64_t n = 0;
+  auto put = [&](int b, int split, int nsplit_b, int kb0, int kb1) {
+    if (rows != nullptr && n < max_rows) {
+      int32_t* r = rows + n * kDecodeScheduleRowWidth;
+      r[0] = b;
+      r[1] = split;
+      r[2] = nsplit_b;
+      r[3] = kb0;
+      r[4] = kb1;
+    }
+    ++n;
+  };
+  if (seq_lens == nullptr) {  // uniform batch: grid (split, kv head, batch)
+    int ns = 1, ck = Sk;
+    decode_plan(B, Hkv, Sk, num_sms, kq4, vq4, &ns, &ck);
+    for (int b = 0; b < B; ++b)
+      for (int sp = 0; sp < ns; ++sp) {
+        const int kb0 = sp * ck;
+        put(b, sp, ns, kb0, kb0 + ck < Sk ? kb0 + ck : Sk);
+      }
+    return n;
+  }
+  const int nt = decode_paged_ctas(B, Hkv, num_sms, kq4, vq4);  // CTAs per kv head
+  for (int c = 0; c < nt; ++c) {
+    PagedSlot ps;
+    if (!paged_slot(seq_lens, B, cap, nt, tile, c, ps)) {
+      put(-1, 0, 0, 0, 0);
+      continue;
+    }
+    const int len = paged_len(seq_lens, ps.b, cap);
+    const int ck = paged_chunk(len, ps.nsplit_b, tile);
+    const int kb0 = ps.split * ck;
+    put(ps.b, ps.split, ps.nsplit_b, kb0, kb0 + ck < len ? kb0 + ck : len);
+  }
+  return n;
 }
 
 uint32_t decode_take_error() {

@@ -66,6 +66,14 @@ void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool kq4, bool vq4, in
 int decode_tile_keys(bool kq4, bool vq4);
 // CTAs per kv head of a paged decode launch (shared over the batch on the device)
 int decode_paged_ctas(int B, int Hkv, int num_sms, bool kq4, bool vq4);
+// the decode kernels' work split computed on the host by the kernels' own plan code: one row of
+// kDecodeScheduleRowWidth values {sequence, split, splits of the sequence, first key, end key}
+// per CTA of one kv head (uniform batch, seq_lens == nullptr: B x nsplit rows; paged batch:
+// seq_lens in host memory, lengths clamped to [1, cap], sequence -1 past the plan); returns
+// the row count
+constexpr int kDecodeScheduleRowWidth = 5;
+int64_t decode_debug_schedule(const int32_t* seq_lens, int B, int Hkv, int Sk, int cap,
+                              bool kq4, bool vq4, int num_sms, int32_t* rows, int64_t max_rows);
 
 // q4_0 quantization of up to two tensors in one launch (job 1 may be absent: x1 == nullptr).
 // Source rows [B*H][S_src][D]; row (bh, s) goes to destination row bh * Scap + pos0 + s.

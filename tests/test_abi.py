@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     assert fa.fa_status_string(0) == "FA_OK"
     assert fa.fa_status_string(4) == "FA_ERR_TIMEOUT"
-    assert fa.fa_version() == 104
+    assert fa.fa_version() == 105
 
 
 def test_q4_0_sizes(lib):
