@@ -69,12 +69,13 @@ typedef enum {
  *                 (Sk - Sq gives the bottom-right aligned chunked-prefill mask)
  *  causal    : nonzero for the causal mask
  *  scale     : softmax scale, finite and > 0 (typically 1/sqrt(D))
- * Sq == 1 runs the split-K decode kernels and needs a scratch buffer of fa_workspace_bytes();
- * fa_fwd takes it from the stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on `stream`);
- * use fa_fwd_ex to pass one instead.  Sq >= 2 runs the prefill kernel; where there are more
- * work units than SMs and cutting them evenly over one CTA per SM is estimated to finish sooner
- * (D = 128), it uses fa_workspace_bytes() of scratch for the partial rows of units
- * cut between CTAs; with less scratch (or none) it runs one unit per CTA. */
+ * Sq == 1 runs the split-K decode kernels and needs a scratch buffer of fa_workspace_bytes().
+ * Sq >= 2 runs the prefill kernel; where there are more work units than SMs and cutting them
+ * evenly over one CTA per SM is estimated to finish sooner (D = 128), it uses
+ * fa_workspace_bytes() of scratch for the partial rows of units cut between CTAs; with less
+ * scratch (or none) it runs one unit per CTA.  fa_fwd takes the scratch from the stream-ordered
+ * allocator (cudaMallocAsync/cudaFreeAsync on `stream`); if that fails, decode returns
+ * FA_ERR_CUDA and prefill runs one unit per CTA.  Use fa_fwd_ex to pass the scratch instead. */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
                  int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
                  fa_dtype dtype, fa_kv_format kv_format, fa_stream_t stream);
@@ -92,8 +93,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, in
  *                 mistaken for this call's only if it holds exactly the call's 32-bit tag.
  *  rescale_count : optional device int32 [B, Hq, Sq] (NULL to skip).  The prefill kernel writes
  *                 for every query row how many times its softmax frame was moved (the first
- *                 key block always sets it, so every value is >= 1); the deferred rescale of
- *                 #2306 fires only on the moves after the first.  Not written when Sq == 1. */
+ *                 key block always sets it, so every value is >= 1); the deferred rescale
+ *                 ("perf(rocm): defer SDPA accumulator rescale, stage Q once per block
+ *                 (#2306)", Summary) fires only on the moves after the first.  Not written
+ *                 when Sq == 1. */
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
                     int Sq, int Sk, int D, int q_pos_offset, int causal, float scale,
                     fa_dtype dtype, fa_kv_format kv_format, void* workspace,

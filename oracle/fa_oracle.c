@@ -17,7 +17,7 @@
  *    "perf(rocm): defer SDPA accumulator rescale, stage Q once per block (#2306)" tests its fused
  *    kernel against (Conversation, second paragraph; What changed), and the SDPA call of
  *    "Build FlashAttention (CK backend) on gfx90a" (Verification).  Grouped-query heads map query
- *    head h to key/value head g(h) = h / (Hq/Hkv) (contiguous groups; the #2306 page's GQA 32/8
+ *    head h to key/value head g(h) = h / (Hq/Hkv) (contiguous groups; that page's GQA 32/8
  *    shape).  The causal mask hides key j from query row i when j > q_pos_offset + i, so a query
  *    chunk placed at positions Sk-Sq..Sk-1 is bottom-right aligned and the diagonal is visible.
  *    The deferred-rescale frame of the fused kernel is NOT modelled: the exact result does not

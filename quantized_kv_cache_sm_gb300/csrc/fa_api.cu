@@ -456,7 +456,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, in
   const size_t need =
       workspace_for(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, q4, q4, nullptr, nullptr);
   void* ws = nullptr;
-  if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess) {
+    // decode cannot run without its split scratch; prefill runs one unit per CTA instead (the
+    // failed allocation's error is cleared so that the launch check does not report it)
+    ws = nullptr;
+    if (Sq == 1) return FA_ERR_CUDA;
+    (void)cudaGetLastError();
+  }
   const fa_status r = fa_fwd_ex(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale,
                                 dtype, kv_format, ws, need, nullptr, stream);
   if (ws && cudaFreeAsync(ws, s) != cudaSuccess && r == FA_OK) return FA_ERR_CUDA;

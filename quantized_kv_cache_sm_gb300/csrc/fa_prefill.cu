@@ -11,17 +11,19 @@
 //    once per block");
 //  * K and V tiles of 128 keys stream through a ring of shared-memory stages, each side either
 //    by TMA (dense f16/bf16 cache) or as q4_0 nibble/scale tiles that dequant warps expand into
-//    the same f16/bf16 swizzled layout (K and V formats are independent template parameters) (the fused K and V dequant of "FlashAttention on gfx90a: Why It's
-//    Broken and How to Fix It", Why FA-off Can't Do V Quantization, point 5); every K/V tile
-//    serves both query tiles;
+//    the same f16/bf16 swizzled layout; K and V formats are independent template parameters.
+//    This is the fused K and V dequant of "FlashAttention on gfx90a: Why It's Broken and How to
+//    Fix It" (Why FA-off Can't Do V Quantization, point 5); every K/V tile serves both query
+//    tiles;
 //  * S = Q K^T and O += P V are tcgen05.mma into tensor memory; the single MMA thread
 //    interleaves the tiles (PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1)) so the tensor core works on
 //    one tile while the softmax warps of the other run;
 //  * the softmax warps own one row each: block max, the deferred rescale, P = 2^(t - f) written
 //    back over S as f16/bf16 for the PV MMA, running row sum l;
-//  * deferred rescale (#2306, kFaWmmaRescaleMargin): a row keeps its frame f until a block max
-//    exceeds f by more than 10 natural-log units; only then are O and l multiplied by
-//    e^(f_old - f_new).  P stays below e^10 = 22026 in every frame.
+//  * deferred rescale ("perf(rocm): defer SDPA accumulator rescale, stage Q once per block
+//    (#2306)", Summary; What changed): a row keeps its frame f until a block max exceeds f by
+//    more than 10 natural-log units; only then are O and l multiplied by e^(f_old - f_new).
+//    P stays below e^10 = 22026 in every frame.
 //
 // Warp roles (12 warps):
 //   warp 0       TMA producer (one lane)
