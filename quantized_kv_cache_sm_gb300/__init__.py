@@ -157,12 +157,40 @@ class Q4Tensor:
         return self.buf.data_ptr()
 
 
+def _check_q4(t: Q4Tensor, what: str):
+    """A Q4Tensor's buffer must be one contiguous uint8 vector holding both planes."""
+    if t.buf.dtype != torch.uint8 or t.buf.dim() != 1 or not t.buf.is_contiguous():
+        raise ValueError(f"{what}: the q4_0 buffer must be a contiguous uint8 vector")
+    need = fa_q4_0_bytes(t.B, t.H, t.S, t.D)
+    if need == 0 or t.buf.numel() < need:
+        raise ValueError(f"{what}: a q4_0 tensor of shape {t.shape} needs {need} bytes, "
+                         f"its buffer holds {t.buf.numel()}")
+
+
+def _on_device(*tensors):
+    """The kernels run on the current CUDA device and take raw pointers: every tensor argument
+    (None skipped) must live there."""
+    cur = None
+    for t in tensors:
+        if t is None:
+            continue
+        d = t.buf.device if isinstance(t, Q4Tensor) else t.device
+        if d.type != "cuda":
+            raise ValueError(f"tensor arguments must be CUDA tensors (one is on {d})")
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if d.index != cur:
+            raise ValueError(f"a tensor is on cuda:{d.index} but the current device is cuda:{cur}")
+
+
 def _kv_args(k, v):
     if isinstance(k, Q4Tensor) != isinstance(v, Q4Tensor):
         raise TypeError("k and v must both be dense tensors or both be Q4Tensor")
     if isinstance(k, Q4Tensor):
         if k.shape != v.shape:
             raise ValueError("k and v shapes differ")
+        _check_q4(k, "k")
+        _check_q4(v, "v")
         return FA_KV_Q4_0, k.shape
     if k.shape != v.shape or k.dim() != 4:
         raise ValueError("k and v must both be [B, Hkv, Sk, D]")
@@ -186,6 +214,7 @@ def _fwd_args(q, k, v, o, causal, q_pos_offset, scale):
         scale = D ** -0.5
     if q_pos_offset is None:
         q_pos_offset = Sk - Sq
+    _on_device(q, k, v, o)
     return (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Sk, D,
             int(q_pos_offset), int(bool(causal)), float(scale), _dtype_code(q.dtype), kv_format)
 
@@ -212,6 +241,7 @@ def fa_fwd_ex(q, k, v, o=None, *, causal: bool = True, q_pos_offset: int | None 
         o = torch.empty_like(q)
     lib = load()
     args = _fwd_args(q, k, v, o, causal, q_pos_offset, scale)
+    _on_device(workspace, rescale_count)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc_ptr = None
@@ -241,6 +271,11 @@ def fa_quantize_q4_0(x: torch.Tensor, out: Q4Tensor | None = None, *, stream=Non
         raise ValueError("x must be a contiguous [B, H, S, D] tensor")
     B, H, S, D = x.shape
     lib = load()
+    if out is not None:
+        if out.shape != (B, H, S, D):
+            raise ValueError("out must be a q4_0 tensor of the shape of x")
+        _check_q4(out, "out")
+    _on_device(x, out)
     if out is None:
         nbytes = fa_q4_0_bytes(B, H, S, D)
         if nbytes == 0:
@@ -344,6 +379,7 @@ def fa_fwd_decode_noalloc(q, k, v, o=None, *, causal: bool = True,
 def _side(t):
     """(format code, [B, H, S, D]) of one K or V operand: a dense tensor or a Q4Tensor."""
     if isinstance(t, Q4Tensor):
+        _check_q4(t, "k/v")
         return FA_KV_Q4_0, tuple(t.shape)
     if t.dim() != 4 or not t.is_contiguous():
         raise ValueError("dense k/v must be contiguous [B, Hkv, S, D] tensors")
@@ -376,6 +412,7 @@ def fa_fwd_kv(q, k, v, o=None, *, Sk: int | None = None, causal: bool = True,
         q_pos_offset = Sk - Sq
     if scale is None:
         scale = D ** -0.5
+    _on_device(q, k, v, o, workspace, rescale_count)
     lib = load()
     if workspace is None:
         need = lib.fa_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, int(q_pos_offset), int(bool(causal)))
@@ -420,6 +457,9 @@ def fa_append_q4_0(k_new: torch.Tensor, k_cache: Q4Tensor, pos0: int,
             raise ValueError("v_new must match k_new")
         if v_cache.shape != k_cache.shape:
             raise ValueError("v_cache must match k_cache")
+        _check_q4(v_cache, "v_cache")
+    _check_q4(k_cache, "k_cache")
+    _on_device(k_new, k_cache, v_new, v_cache)
     _check(load().fa_append_q4_0(k_new.data_ptr(), v_new.data_ptr() if v_new is not None else None,
                                  k_cache.data_ptr(),
                                  v_cache.data_ptr() if v_cache is not None else None, B, H, S_new,
@@ -453,6 +493,7 @@ def fa_decode_paged(q, k_pages, v_pages, block_table: torch.Tensor, seq_lens: to
     if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,):
         raise ValueError("seq_lens must be an int32 [B] tensor")
     pps = block_table.shape[1]
+    _on_device(q, k_pages, v_pages, o, block_table, seq_lens, workspace)
     lib = load()
     if workspace is None:
         need = lib.fa_decode_paged_workspace_bytes(B, Hq, Hkv, D, page, pps)
@@ -487,6 +528,7 @@ def fa_fwd_explicit(q, k, v, o=None, *, causal: bool = True, q_pos_offset: int |
         q_pos_offset = Sk - Sq
     if scale is None:
         scale = D ** -0.5
+    _on_device(q, k, v, o, workspace)
     lib = load()
     if workspace is None:
         need = lib.fa_explicit_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, kf, vf)

@@ -31,3 +31,15 @@ def fa():
 
     fa_mod.load()
     return fa_mod
+
+
+@pytest.fixture(scope="session")
+def built():
+    """The product binding with its library built and loaded; no device needed (host queries and
+    argument checks only)."""
+    import quantized_kv_cache_sm_gb300 as fa_mod
+    from quantized_kv_cache_sm_gb300 import build as fa_build
+
+    fa_build.build()
+    fa_mod.load()
+    return fa_mod

@@ -15,6 +15,11 @@ import pytest
 import quantized_kv_cache_sm_gb300 as fa
 
 
+@pytest.fixture(autouse=True)
+def _library(built):
+    return built
+
+
 def tile_keys(kf, vf):
     return 128 if "q4_0" in (kf, vf) else 64
 

@@ -15,6 +15,12 @@ import pytest
 
 import quantized_kv_cache_sm_gb300 as fa
 
+
+@pytest.fixture(autouse=True)
+def _library(built):
+    return built
+
+
 BM = BN = 128
 
 
