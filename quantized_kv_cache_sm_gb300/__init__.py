@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import dataclasses
+import functools
 import os
 import threading
 
@@ -174,13 +175,15 @@ def _on_device(*tensors):
     for t in tensors:
         if t is None:
             continue
-        d = t.buf.device if isinstance(t, Q4Tensor) else t.device
-        if d.type != "cuda":
-            raise ValueError(f"tensor arguments must be CUDA tensors (one is on {d})")
+        if isinstance(t, Q4Tensor):
+            t = t.buf
+        idx = t.get_device()  # -1 for host memory
+        if idx < 0:
+            raise ValueError(f"tensor arguments must be CUDA tensors (one is on {t.device})")
         if cur is None:
             cur = torch.cuda.current_device()
-        if d.index != cur:
-            raise ValueError(f"a tensor is on cuda:{d.index} but the current device is cuda:{cur}")
+        if idx != cur:
+            raise ValueError(f"a tensor is on cuda:{idx} but the current device is cuda:{cur}")
 
 
 def _kv_args(k, v):
@@ -257,8 +260,14 @@ def fa_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal) -> int:
     return int(load().fa_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, int(bool(causal))))
 
 
-def fa_q4_0_bytes(B, H, S, D) -> int:
+@functools.lru_cache(maxsize=256)
+def _q4_0_bytes(B: int, H: int, S: int, D: int) -> int:
     return int(load().fa_q4_0_bytes(B, H, S, D))
+
+
+def fa_q4_0_bytes(B, H, S, D) -> int:
+    # a pure function of the shape, asked on every call that takes a q4_0 tensor: cached
+    return _q4_0_bytes(int(B), int(H), int(S), int(D))
 
 
 def fa_q4_0_scale_offset(B, H, S, D) -> int:
