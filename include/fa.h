@@ -18,9 +18,12 @@
  * Gap) describes as what the flash-attention path provides.
  *
  * Conventions shared by every entry point
- *  - All tensors are device memory owned by the caller, contiguous, head-major:
+ *  - All tensors are device memory of the current device (the kernels launch there), owned by
+ *    the caller, contiguous, head-major:
  *      Q, O : [B, Hq, Sq, D]        K, V (dense) : [B, Hkv, Sk, D]   (dtype of Q)
- *    Every pointer must be 16-byte aligned.
+ *    Every pointer must be 16-byte aligned.  The entry points check alignment and sizes but
+ *    cannot tell host memory or another device's memory from the current device's: such a
+ *    pointer is undefined behaviour (the Python binding refuses those tensors before calling).
  *  - q4_0 tensor (one buffer per K or V, built by fa_quantize_q4_0), for a [B, H, S, D] source:
  *      nibble plane [B, H, S, D/2] uint8 at offset 0: byte j of each 32-element block holds
  *        element j in its low nibble and element j+16 in its high nibble;
