@@ -71,3 +71,24 @@ def test_reference_arm_line(capsys):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["unit"] == line["unit"]
+
+
+def test_traffic_table_entries_match_what_bench_looks_up():
+    """Every line of profiles/dram_traffic.txt names a kernel key bench.py asks for (kernel,
+    dtype, K/V format) and an existing workload, so a capture cannot be silently orphaned by a
+    typo (whether its source hash is current is a separate matter: a stale one reports null)."""
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles",
+                        "dram_traffic.txt")
+    entries = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert entries
+    asked = {("decode_split_kernel_f16_q4_0", bench.DECODE_WORKLOAD)}
+    for kernel in ("prefill_kernel", "prefill_seg_kernel"):
+        for name, w in fa_inputs.WORKLOADS.items():
+            asked.add((f"{kernel}_{w.dtype}_{w.kv_format}", name))
+    for e in entries:
+        assert len(e) >= 5, e
+        key, srcs, sha, nbytes, workload = e[:5]
+        assert (key, workload) in asked, e
+        assert len(sha) == 16 and int(nbytes) > 0
+        for f in srcs.split("+"):
+            assert os.path.exists(os.path.join(bench.ROOT, "quantized_kv_cache_sm_gb300", "csrc", f))
