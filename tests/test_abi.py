@@ -67,6 +67,18 @@ def test_prefill_workspace_without_a_device(lib):
     assert fa.fa_workspace_bytes(1, 32, 7, 2, 16, 128, 0, 1) == 0  # invalid: Hq % Hkv
 
 
+def test_decode_workspace_layout_without_a_device(lib):
+    # with no device the decode plan has no SMs to fill and uses one split per (batch, kv head):
+    # the scratch is the arrival flags [B, Hkv, 1] u32 padded to 256 bytes, then the partials
+    # [B, Hq, 1, D + 4] f32 (m, l, two pads, O)
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    for B, Hq, Hkv, Sk, D in [(4, 32, 8, 65536, 128), (1, 8, 8, 1, 64), (3, 12, 4, 999, 128)]:
+        flags = -(-(B * Hkv * 4) // 256) * 256
+        want = flags + B * Hq * (D + 4) * 4
+        assert fa.fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, Sk - 1, 1) == want
+
+
 P = 1 << 20  # a 16-byte aligned fake device address; never dereferenced by these calls
 
 
