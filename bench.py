@@ -262,7 +262,8 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step": round(ms, 4),
         "higher_is_better": True,
         "scaling": "weak",
-        "vs_baseline": round(value / PAGES_TFLOPS_16K_F16, 1) if args.workload == DEFAULT_WORKLOAD else None,
+        "vs_baseline": (round(value / PAGES_TFLOPS_16K_F16, 1)
+                        if args.workload == DEFAULT_WORKLOAD else None),
         "dtype": w.dtype,
         "data": "synthetic",
         "config": {

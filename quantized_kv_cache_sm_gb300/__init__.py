@@ -249,7 +249,8 @@ def fa_fwd_ex(q, k, v, o=None, *, causal: bool = True, q_pos_offset: int | None 
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc_ptr = None
     if rescale_count is not None:
-        if rescale_count.dtype != torch.int32 or rescale_count.numel() != q.shape[0] * q.shape[1] * q.shape[2]:
+        rows = q.shape[0] * q.shape[1] * q.shape[2]
+        if rescale_count.dtype != torch.int32 or rescale_count.numel() != rows:
             raise ValueError("rescale_count must be int32 [B, Hq, Sq]")
         rc_ptr = rescale_count.data_ptr()
     _check(lib.fa_fwd_ex(*args, ws_ptr, ws_bytes, rc_ptr, _stream(stream)), "fa_fwd_ex")

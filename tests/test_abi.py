@@ -126,7 +126,8 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
 @pytest.mark.parametrize("args,expect", [
     # q, k, v, o, B, Hq, Hkv, Sq, Sk, cap, D, off, causal, scale, dtype, kf, vf
-    ((P, P, P, P, 1, 8, 2, 4, 64, 32, 64, 60, 1, 0.125, 0, 0, 1), fa.FA_ERR_INVALID_ARG),  # cap < Sk
+    # kv_capacity < Sk
+    ((P, P, P, P, 1, 8, 2, 4, 64, 32, 64, 60, 1, 0.125, 0, 0, 1), fa.FA_ERR_INVALID_ARG),
     ((P, P, P, P, 1, 8, 2, 4, 64, 64, 64, 60, 1, 0.125, 0, 0, 7), fa.FA_ERR_INVALID_ARG),  # v fmt
     ((P, P, P, P, 1, 8, 2, 4, 64, 64, 64, 60, 1, 0.125, 0, 3, 1), fa.FA_ERR_INVALID_ARG),  # k fmt
     ((P, P, P, P, 1, 8, 2, 4, 64, 64, 96, 60, 1, 0.125, 0, 1, 0), fa.FA_ERR_UNSUPPORTED),  # D

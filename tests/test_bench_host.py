@@ -91,4 +91,5 @@ def test_traffic_table_entries_match_what_bench_looks_up():
         assert (key, workload) in asked, e
         assert len(sha) == 16 and int(nbytes) > 0
         for f in srcs.split("+"):
-            assert os.path.exists(os.path.join(bench.ROOT, "quantized_kv_cache_sm_gb300", "csrc", f))
+            src = os.path.join(bench.ROOT, "quantized_kv_cache_sm_gb300", "csrc", f)
+            assert os.path.exists(src)
