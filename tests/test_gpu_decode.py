@@ -34,7 +34,8 @@ def run_decode(fa, B, Hq, Hkv, Sk, D, causal, off, dtype, kv, seed, use_ws=True)
     else:
         want = oracle.attention(np64(q), np64(k), np64(v), causal=causal, q_pos_offset=off,
                                 scale=scale)
-    return check_close(np64(o), want, dtype, f"decode B{B} H{Hq}/{Hkv} Sk{Sk} D{D} {dtype} {kv}")
+    return check_close(np64(o), want, dtype, f"decode B{B} H{Hq}/{Hkv} Sk{Sk} D{D} {dtype} {kv}",
+                       q4=kv == "q4_0")
 
 
 CASES = [
@@ -131,3 +132,28 @@ def test_decode_replayed_from_a_cuda_graph(fa):
         torch.cuda.synchronize()
         assert torch.equal(os_, want), seed
     assert fa.fa_get_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("recipe", ["ramp", "q_times_8"])
+def test_decode_large_magnitude_queries(fa, recipe):
+    """The q4_0 decode feeds the K nibbles to the tensor core as offset values (1024 + q and
+    1024 + 16 q in f16) and removes the offset by starting each block's sum at -(offset * sum
+    of the block's Q elements), a cancellation in f32 that grows with |Q|.  Large query
+    magnitudes: the score-ramp recipe at one query per sequence (Q[..., 0] = 8 and a key column
+    rising 2.0 per 128 keys in scaled-score units), and N(0,1) queries multiplied by 8 (scores
+    8x larger, a sharply peaked softmax).  Every output element against the oracle."""
+    B, Hq, Hkv, D = 2, 32, 8, 128
+    Sk = 16384 if recipe == "ramp" else 32768
+    q, k, v = fa_inputs.make_tensors(B, Hq, Hkv, 1, Sk, D, "f16", seed=61,
+                                     ramp=recipe == "ramp")
+    if recipe == "q_times_8":
+        q = (q.float() * 8.0).to(q.dtype)
+    kd, vd = fa.fa_quantize_q4_0(k.cuda()), fa.fa_quantize_q4_0(v.cuda())
+    ws = torch.empty(fa.fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, Sk - 1, True),
+                     dtype=torch.uint8, device="cuda")
+    o = fa.fa_fwd_ex(q.cuda(), kd, vd, causal=True, q_pos_offset=Sk - 1, scale=D ** -0.5,
+                     workspace=ws)
+    assert fa.fa_get_status() == fa.FA_OK
+    want = oracle.attention_q4_0(np64(q), oracle_q4_planes(k), oracle_q4_planes(v), causal=True,
+                                 q_pos_offset=Sk - 1, scale=D ** -0.5)
+    check_close(np64(o), want, "f16", f"decode, large queries ({recipe})", q4=True)

@@ -1,10 +1,11 @@
 """The explicit (non-flash) path, fa_fwd_explicit, against the f64 oracle through the C ABI, and
 against the fused path on the same inputs.  Tolerance: max-abs 1e-2 (f16) / 2e-2 (bf16)."""
+import numpy as np
 import pytest
 
 import fa_inputs
 import oracle
-from gpu_common import check_close, np64, oracle_q4_planes
+from gpu_common import check_close, np64, oracle_q4_planes, rel_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +36,9 @@ def test_explicit_path_matches_oracle(fa, case):
     o = fa.fa_fwd_explicit(q.cuda(), kd, vd, causal=causal, q_pos_offset=off, scale=D ** -0.5)
     assert fa.fa_get_status() == fa.FA_OK
     want = oracle.attention(np64(q), k64, v64, causal=causal, q_pos_offset=off, scale=D ** -0.5)
-    check_close(np64(o), want, dtype, f"explicit {case}")
+    q4 = "q4_0" in (kf, vf)
+    check_close(np64(o), want, dtype, f"explicit {case}", q4=q4)
     fused = fa.fa_fwd_kv(q.cuda(), kd, vd, causal=causal, q_pos_offset=off, scale=D ** -0.5)
-    check_close(np64(o), np64(fused), dtype, "explicit vs fused")
+    # two GPU results, each within the bound of the oracle: their difference within twice it
+    ratio = np.abs(np64(o) - np64(fused)) / (2 * rel_bound(want, dtype, q4))
+    assert ratio.max() <= 1.0, ("explicit vs fused", float(ratio.max()))

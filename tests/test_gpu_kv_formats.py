@@ -45,7 +45,7 @@ def test_mixed_formats_match_oracle(fa, case):
     o = fa.fa_fwd_kv(q.cuda(), kd, vd, causal=causal, q_pos_offset=off, scale=D ** -0.5)
     assert fa.fa_get_status() == fa.FA_OK
     want = oracle.attention(np64(q), k64, v64, causal=causal, q_pos_offset=off, scale=D ** -0.5)
-    check_close(np64(o), want, dtype, f"{kf} K / {vf} V {case}")
+    check_close(np64(o), want, dtype, f"{kf} K / {vf} V {case}", q4="q4_0" in (kf, vf))
 
 
 @pytest.mark.parametrize("fmt", [("dense", "dense"), ("q4_0", "q4_0"), ("dense", "q4_0")])
@@ -65,7 +65,7 @@ def test_cache_larger_than_filled_length(fa, fmt, Sq):
     assert fa.fa_get_status() == fa.FA_OK
     want = oracle.attention(np64(q), kf64, vf64, causal=True, q_pos_offset=Sk - Sq,
                             scale=D ** -0.5)
-    check_close(np64(o), want, "f16", f"capacity {cap} > Sk {Sk}, {fmt}")
+    check_close(np64(o), want, "f16", f"capacity {cap} > Sk {Sk}, {fmt}", q4="q4_0" in fmt)
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
@@ -109,7 +109,7 @@ def test_append_then_chunked_prefill_over_the_cache(fa):
         rows = sample_rows(B, Hq, 1024, per_head=8, seed=c0)
         want = oracle.attention_q4_0(np64(qc), kp, vp, causal=True, q_pos_offset=c0,
                                      scale=D ** -0.5, rows=rows)
-        check_close(np64(o).reshape(-1, D)[rows], want, "f16", f"chunk at {c0}")
+        check_close(np64(o).reshape(-1, D)[rows], want, "f16", f"chunk at {c0}", q4=True)
 
 
 def test_fwd_kv_with_equal_formats_equals_fa_fwd_ex(fa):
@@ -119,3 +119,45 @@ def test_fwd_kv_with_equal_formats_equals_fa_fwd_ex(fa):
     b = fa.fa_fwd_kv(q, kq, vq)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_mixed_decode_at_the_benchmarked_size(fa):
+    """f16 K with a q4_0 V, 4 sequences x 65 536 keys, GQA 32/8, D = 128: the benchmark's mixed
+    decode leg, every output element against the oracle (one sequence at a time, so the f64
+    copies stay a few hundred MB)."""
+    w = fa_inputs.WORKLOADS["decode_q4_0_b4_gqa32x8_d128_sk65536_f16"]
+    q, k, v = fa_inputs.make_qkv(w)
+    vd = fa.fa_quantize_q4_0(v.cuda())
+    ws = torch.empty(fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, 1, w.Sk, w.D, w.q_pos_offset, True),
+                     dtype=torch.uint8, device="cuda")
+    o = fa.fa_fwd_kv(q.cuda(), k.cuda(), vd, causal=True, q_pos_offset=w.q_pos_offset,
+                     workspace=ws)
+    assert fa.fa_get_status() == fa.FA_OK
+    got = np64(o)
+    for b in range(w.B):
+        vn, vs = oracle_q4_planes(v[b:b + 1].contiguous())
+        want = oracle.attention(np64(q[b:b + 1]), np64(k[b:b + 1]), oracle.dequantize_q4_0(vn, vs),
+                                causal=True, q_pos_offset=w.q_pos_offset, scale=w.scale)
+        check_close(got[b:b + 1], want, w.dtype, f"f16 K + q4_0 V decode, sequence {b}", q4=True)
+
+
+def test_append_at_the_benchmarked_size(fa):
+    """The benchmark's append leg: a 16 384-token chunk of K and V (B 4, 8 heads, D 128) written
+    at position 32 768 of q4_0 caches of 65 536 tokens.  The written planes are bit-exact against
+    the oracle's quantizer; every byte outside the chunk keeps its fill."""
+    B, H, D, cap, pos0, n = 4, 8, 128, 65536, 32768, 16384
+    kn = fa_inputs.make_tensors(B, H, H, 1, n, D, "f16", seed=71)[1]
+    vn = fa_inputs.make_tensors(B, H, H, 1, n, D, "f16", seed=73)[1]
+    kc, vc = fa.q4_0_cache(B, H, cap, D), fa.q4_0_cache(B, H, cap, D)
+    kc.buf.fill_(0x3C)
+    vc.buf.fill_(0xC3)
+    fa.fa_append_q4_0(kn.cuda(), kc, pos0, vn.cuda(), vc)
+    assert fa.fa_get_status() == fa.FA_OK
+    for cache, src, fill in ((kc, kn, 0x3C), (vc, vn, 0xC3)):
+        nib, sc = q4_planes_gpu(cache)
+        want_nib, want_sc = oracle_q4_planes(src)
+        assert np.array_equal(nib[:, :, pos0:pos0 + n], want_nib)
+        assert np.array_equal(sc[:, :, pos0:pos0 + n], want_sc)
+        for lo, hi in ((0, pos0), (pos0 + n, cap)):
+            assert (nib[:, :, lo:hi] == fill).all()
+            assert (sc[:, :, lo:hi] == (fill | (fill << 8))).all()

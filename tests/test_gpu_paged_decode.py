@@ -74,7 +74,8 @@ def test_paged_varlen_decode_matches_oracle(fa, case):
         ks, vs = seqs[b]
         want = oracle.attention(np64(q[b:b + 1]), ks[None], vs[None], causal=False,
                                 scale=D ** -0.5)
-        check_close(got[b:b + 1], want, dtype, f"sequence {b} ({lens[b]} keys)")
+        check_close(got[b:b + 1], want, dtype, f"sequence {b} ({lens[b]} keys)",
+                    q4="q4_0" in (kf, vf))
 
 
 def test_paged_decode_repeated_calls_and_stale_workspace(fa):
@@ -108,3 +109,49 @@ def test_bad_page_number_and_length_are_reported_not_read(fa):
     assert fa.fa_get_status() == fa.FA_ERR_INVALID_ARG
     fa.fa_decode_paged(q, kd, vd, table, torch.tensor(lens, dtype=torch.int32, device="cuda"))
     assert fa.fa_get_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("lens", [[65536] * 4, [65536, 32768, 16384, 8192]],
+                         ids=["65536x4", "varlen_65536_32768_16384_8192"])
+def test_paged_decode_at_the_benchmarked_sizes(fa, lens):
+    """The benchmark's paged legs: q4_0 K and V pools of 256-token pages in shuffled order, GQA
+    32/8, D = 128, every output element against the oracle.  The oracle takes each sequence's
+    pages, gathered in order, as q4_0 planes of its own quantizer (nothing is expanded to f64
+    beyond one key at a time)."""
+    Hq, Hkv, D, page = 32, 8, 128, 256
+    B = len(lens)
+    npages = [n // page for n in lens]
+    NP = sum(npages)
+    g = torch.Generator().manual_seed(1006)
+    perm = torch.randperm(NP, generator=g)
+    table = torch.zeros(B, max(npages), dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(npages):
+        table[b, :n] = perm[at:at + n].to(torch.int32)
+        at += n
+    kpool = torch.randn(NP, Hkv, page, D, generator=g).to(torch.float16)
+    vpool = torch.randn(NP, Hkv, page, D, generator=g).to(torch.float16)
+    q = torch.randn(B, Hq, 1, D, generator=g).to(torch.float16)
+    kd, vd = fa.fa_quantize_q4_0(kpool.cuda()), fa.fa_quantize_q4_0(vpool.cuda())
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    tab = table.cuda()
+    ws = torch.empty(fa.load().fa_decode_paged_workspace_bytes(B, Hq, Hkv, D, page,
+                                                              table.shape[1]),
+                     dtype=torch.uint8, device="cuda")
+    o = fa.fa_decode_paged(q.cuda(), kd, vd, tab, sl, workspace=ws)
+    assert fa.fa_get_status() == fa.FA_OK
+    got = np64(o)
+    kn, ks = oracle_q4_planes(kpool)
+    del kpool
+    vn, vs = oracle_q4_planes(vpool)
+    del vpool
+    for b, n in enumerate(lens):
+        pages = table[b, :npages[b]].numpy()
+
+        def seq(plane):  # [pages, Hkv, page, X] -> [1, Hkv, n, X]
+            return np.ascontiguousarray(plane[pages].transpose(1, 0, 2, 3)
+                                        .reshape(Hkv, -1, plane.shape[-1])[None, :, :n])
+
+        want = oracle.attention_q4_0(np64(q[b:b + 1]), (seq(kn), seq(ks)), (seq(vn), seq(vs)),
+                                     causal=True, q_pos_offset=n - 1, scale=D ** -0.5)
+        check_close(got[b:b + 1], want, "f16", f"paged sequence {b} ({n} keys)", q4=True)

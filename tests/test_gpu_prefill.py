@@ -1,8 +1,11 @@
 """Prefill kernel (Sq >= 2) against the f64 oracle, through the C ABI.
 
-Small and ragged shapes are compared on every output element; the full-size chunked-prefill
-workloads on sampled rows (tile edges, last rows, random rows of every head) in the same launch
-configuration the benchmark times.  Tolerance: max-abs 1e-2 (f16) / 2e-2 (bf16)."""
+Small and ragged shapes are compared on every output element.  The full-size chunked-prefill
+workloads are compared here on sampled rows (tile edges, last rows, random rows of every head)
+with the per-row frame-move counts, through the one-unit-per-CTA launch (no scratch passed);
+tests/test_gpu_prefill_full.py compares every row of them, through both the one-unit-per-CTA
+launch and the cut-schedule launch the benchmark times.  Tolerance: the absolute and relative
+bounds of gpu_common."""
 import numpy as np
 import pytest
 import torch
@@ -37,7 +40,8 @@ def run_case(fa, B, Hq, Hkv, Sq, Sk, D, causal, off, dtype, kv, seed, rows=None,
     got = np64(o)
     if rows is not None:
         got = got.reshape(-1, D)[rows]
-    err = check_close(got, want, dtype, f"B{B} H{Hq}/{Hkv} Sq{Sq} Sk{Sk} D{D} {dtype} {kv}")
+    err = check_close(got, want, dtype, f"B{B} H{Hq}/{Hkv} Sq{Sq} Sk{Sk} D{D} {dtype} {kv}",
+                      q4=kv == "q4_0")
     return err, (rc.cpu().numpy() if counts else None)
 
 

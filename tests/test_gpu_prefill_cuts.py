@@ -164,6 +164,7 @@ def test_cut_schedule_q4_0_caches(fa, fmt):
     rows = sample_rows(w.B, w.Hq, w.Sq, per_head=8, seed=5)
     want = oracle.attention(np64(q), k64, v64, causal=True, q_pos_offset=w.q_pos_offset,
                             scale=w.scale, rows=rows)
-    check_close(np64(o_cut).reshape(-1, w.D)[rows], want, w.dtype, f"{fmt} cut schedule")
+    check_close(np64(o_cut).reshape(-1, w.D)[rows], want, w.dtype, f"{fmt} cut schedule",
+                q4=True)
     diff = (o_cut.float() - o_whole.float()).abs().max().item()
     assert diff <= 4e-3, diff
