@@ -140,14 +140,18 @@ size_t fa_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_p
  * FA_NOALLOC_SCRATCH_BYTES that the library itself holds on every GPU that loads it, until the
  * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *  Arguments: as fa_fwd with Sq = 1 (q, o: [B, Hq, 1, D]; k, v: [B, Hkv, Sk, D] dense or q4_0).
- *  Limit: shapes whose fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal) exceeds
- *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED.  That size is
- *    4 * B * Hkv * nsplit rounded up to a multiple of 256, plus 4 * (D + 4) * B * Hq * nsplit,
- *    nsplit being the split count the decode plan picks (about 3 * SM count / (B * Hkv), at
- *    least 1): for D = 128 roughly B * Hq * nsplit <= 7900.  Invalid shapes give
- *    FA_ERR_INVALID_ARG.
+ *  Limit: a shape is accepted exactly when
+ *      fa_workspace_bytes(B, Hq, Hkv, 1, Sk, D, q_pos_offset, causal) <= FA_NOALLOC_SCRATCH_BYTES
+ *    -- that query is the largest need over every pair of cache formats, so the answer does not
+ *    depend on kv_format -- and rejected with FA_ERR_UNSUPPORTED otherwise.  The need grows
+ *    with B * Hq times the split count the decode plan picks for the device (about
+ *    3 * SM count / (B * Hkv), at least 1, at most the key tiles), so call fa_workspace_bytes
+ *    to know whether a shape fits.  Invalid shapes give FA_ERR_INVALID_ARG.
  *  First call per device: it looks up the array's device address (cudaGetSymbolAddress) with
- *    that device current, so make the first call on each device before any stream capture.
+ *    that device current, so make the first call on each device before any stream capture.  The
+ *    address is kept per device together with the context it was looked up in, and looked up
+ *    again when a call finds another context current (after cudaDeviceReset, say): that call
+ *    too should not be captured.
  *  Sharing: every call on a device uses the same array and leaves its contents behind.  Nothing
  *    in it needs clearing (see the workspace of fa_fwd_ex), but calls whose
  *    execution overlaps on the GPU -- on different streams, or from different host threads --

@@ -8,6 +8,8 @@
 // the caller to find that memory.  fa_fwd_decode_noalloc instead uses a fixed scratch area that
 // lives in this file as a `static __device__` array: every GPU that loads the library holds it
 // (FA_NOALLOC_SCRATCH_BYTES) until the process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -26,7 +28,26 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchBytes / 
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
+// device address of g_noalloc_scratch, per device, and the context it was looked up in: a
+// context that is destroyed and created again (cudaDeviceReset) loads the module afresh, so the
+// address is looked up again whenever the current context differs from the recorded one
+void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current_fn() {
+  static std::once_flag once;
+  static CtxGetCurrentFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
 
 }  // namespace
 }  // namespace fa
@@ -42,13 +63,25 @@ extern "C" fa_status fa_fwd_decode_noalloc(const void* q, const void* k, const v
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   {
-    // one-time set-up per device, with that device current: look up where the array lives
+    // one-time set-up per device (and context), with that device current: look up where the
+    // array lives.  If no context is bound to this thread yet, cudaSetDevice binds the device's
+    // primary context (it initialises it, allocating nothing), so that the context read here is
+    // the one the lookup and the launch use.
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (get_ctx == nullptr) return FA_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return FA_ERR_CUDA;
+    if (ctx == nullptr) {
+      if (cudaSetDevice(dev) != cudaSuccess || get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return FA_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    if (g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
         return FA_ERR_CUDA;
       g_scratch_addr[dev] = p;
+      g_scratch_ctx[dev] = ctx;
     }
     scratch = g_scratch_addr[dev];
   }
