@@ -177,16 +177,19 @@ __device__ __forceinline__ float block_row_max(uint32_t scol, int rel_lim) {
     reg_fence32(r1);
     float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float a = __uint_as_float(r0[i]), c = __uint_as_float(r1[i]);
+    for (int i = 0; i < 32; i += 2) {
+      float a0 = __uint_as_float(r0[i]), a1 = __uint_as_float(r0[i + 1]);
+      float c0 = __uint_as_float(r1[i]), c1 = __uint_as_float(r1[i + 1]);
       if (MASK) {
-        if (64 * hf + i > rel_lim) a = -INFINITY;
-        if (64 * hf + 32 + i > rel_lim) c = -INFINITY;
+        if (64 * hf + i > rel_lim) a0 = -INFINITY;
+        if (64 * hf + i + 1 > rel_lim) a1 = -INFINITY;
+        if (64 * hf + 32 + i > rel_lim) c0 = -INFINITY;
+        if (64 * hf + 33 + i > rel_lim) c1 = -INFINITY;
       }
-      m0 = fmaxf(m0, a);
-      m1 = fmaxf(m1, c);
+      m0 = fmax3(m0, a0, a1);
+      m1 = fmax3(m1, c0, c1);
     }
-    mx = fmaxf(mx, fmaxf(m0, m1));
+    mx = fmax3(mx, m0, m1);
   }
   return mx;
 }
@@ -195,7 +198,9 @@ __device__ __forceinline__ float block_row_max(uint32_t scol, int rel_lim) {
 // returns the row sum of P.
 template <bool MASK, bool BF16>
 __device__ __forceinline__ float block_row_exp(uint32_t scol, int rel_lim, float sl2, float nf) {
-  float la = 0.f, lb = 0.f;
+  // the scale-and-shift and the row sum run two keys per instruction (packed f32 pairs)
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), nfx2 = f2_pack(nf, nf);
+  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t r[32];
@@ -210,13 +215,16 @@ __device__ __forceinline__ float block_row_exp(uint32_t scol, int rel_lim, float
         if (32 * c + 2 * i > rel_lim) s0 = -INFINITY;
         if (32 * c + 2 * i + 1 > rel_lim) s1 = -INFINITY;
       }
-      const float p0 = ex2(fmaf(s0, sl2, nf)), p1 = ex2(fmaf(s1, sl2, nf));
-      if (i & 1) lb += p0 + p1; else la += p0 + p1;
+      const float2 t = f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, nfx2));
+      const float p0 = ex2(t.x), p1 = ex2(t.y);
+      const uint64_t pp = f2_pack(p0, p1);
+      if (i & 1) acc1 = f2_add(acc1, pp); else acc0 = f2_add(acc0, pp);
       pr[i] = pack2<BF16>(p0, p1);
     }
     tmem_st16(scol + 16 * c, pr);
   }
-  return la + lb;
+  const float2 a = f2_unpack(f2_add(acc0, acc1));
+  return a.x + a.y;
 }
 
 // Single-read form of the two passes above: the row's 128 scores of S(j) read from TMEM with
@@ -234,7 +242,6 @@ __device__ __forceinline__ float block_row_load(uint32_t scol, int rel_lim, floa
   reg_fence32(r1);
   reg_fence32(r2);
   reg_fence32(r3);
-  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     s[i] = __uint_as_float(r0[i]);
@@ -247,30 +254,40 @@ __device__ __forceinline__ float block_row_load(uint32_t scol, int rel_lim, floa
       if (64 + i > rel_lim) s[64 + i] = -INFINITY;
       if (96 + i > rel_lim) s[96 + i] = -INFINITY;
     }
-    m0 = fmaxf(m0, s[i]);
-    m1 = fmaxf(m1, s[32 + i]);
-    m2 = fmaxf(m2, s[64 + i]);
-    m3 = fmaxf(m3, s[96 + i]);
   }
-  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  // four independent chains, two new scores per three-input max
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    m0 = fmax3(m0, s[i], s[i + 1]);
+    m1 = fmax3(m1, s[32 + i], s[33 + i]);
+    m2 = fmax3(m2, s[64 + i], s[65 + i]);
+    m3 = fmax3(m3, s[96 + i], s[97 + i]);
+  }
+  return fmax3(fmaxf(m0, m1), m2, m3);
 }
 template <bool BF16>
 __device__ __forceinline__ float block_row_exp_regs(uint32_t scol, const float (&s)[kBN],
                                                     float sl2, float nf) {
-  float la = 0.f, lb = 0.f;
+  // the scale-and-shift and the row sum run two keys per instruction (packed f32 pairs)
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), nfx2 = f2_pack(nf, nf);
+  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t pr[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float p0 = ex2(fmaf(s[32 * c + 2 * i], sl2, nf));
-      const float p1 = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, nf));
-      if (i & 1) lb += p0 + p1; else la += p0 + p1;
+      const float2 t =
+          f2_unpack(f2_fma(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, nfx2));
+      const float p0 = ex2(t.x), p1 = ex2(t.y);
+      const uint64_t pp = f2_pack(p0, p1);
+      if (i & 1) acc1 = f2_add(acc1, pp); else acc0 = f2_add(acc0, pp);
       pr[i] = pack2<BF16>(p0, p1);
     }
     tmem_st16(scol + 16 * c, pr);
   }
-  return la + lb;
+  const float2 a = f2_unpack(f2_add(acc0, acc1));
+  return a.x + a.y;
 }
 
 // One key block of the online softmax for this thread's query row: read S(j), move the frame f
