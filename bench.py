@@ -407,10 +407,13 @@ def other_legs(fa, dev, stream, flush, peaks):
         if w.kv_format == "q4_0":
             k, v = fa.fa_quantize_q4_0(k), fa.fa_quantize_q4_0(v)
         o = torch.empty_like(q)
+        # the call's scratch is allocated once, outside the timed loop, as for the headline leg
+        n = fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset, w.causal)
+        ws = torch.empty(n, dtype=torch.uint8, device=dev) if n > 0 else None
 
         def call():
-            fa.fa_fwd(q, k, v, o, causal=True, q_pos_offset=w.q_pos_offset, scale=w.scale,
-                      stream=stream)
+            fa.fa_fwd_ex(q, k, v, o, causal=True, q_pos_offset=w.q_pos_offset, scale=w.scale,
+                         workspace=ws, stream=stream)
 
         ms = time_calls(call, 50, 5, flush=flush, stream=stream)
         tf = w.flops() / (ms * 1e-3) / 1e12
@@ -449,6 +452,35 @@ def other_legs(fa, dev, stream, flush, peaks):
         "frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
         "kv_bytes_per_call": nbytes}
     del q, k, vq, o
+    # the chunk appended to q4_0 caches inside the prefill launch, against the two-launch flow
+    # (append, then the prefill over the cache): the q4_0 16K workload's last 2048 tokens are
+    # the chunk, the caches hold the 14336 tokens before it
+    w = fa_inputs.WORKLOADS["prefill_q4_0_gqa32x8_d128_sq2048_sk16384_f16"]
+    q, k, v = fa_inputs.make_qkv(w, device=dev, generate_on_device=True)
+    pos0 = w.q_pos_offset
+    kc, vc = fa.q4_0_cache(w.B, w.Hkv, w.Sk, w.D), fa.q4_0_cache(w.B, w.Hkv, w.Sk, w.D)
+    fa.fa_append_q4_0(k[:, :, :pos0].contiguous(), kc, 0, v[:, :, :pos0].contiguous(), vc)
+    kn, vn = k[:, :, pos0:].contiguous(), v[:, :, pos0:].contiguous()
+    del k, v
+    o = torch.empty_like(q)
+    ws = torch.empty(max(16, fa.fa_prefill_append_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk,
+                                                                  w.D, pos0)),
+                     dtype=torch.uint8, device=dev)
+    ms_fused = time_calls(lambda: fa.fa_prefill_append_q4_0(q, kn, vn, kc, vc, pos0, o,
+                                                            workspace=ws, stream=stream),
+                          50, 5, flush=flush, stream=stream)
+
+    def two_launches():
+        fa.fa_append_q4_0(kn, kc, pos0, vn, vc, stream=stream)
+        fa.fa_fwd_kv(q, kc, vc, o, Sk=w.Sk, causal=True, q_pos_offset=pos0, workspace=ws,
+                     stream=stream)
+
+    ms_two = time_calls(two_launches, 50, 5, flush=flush, stream=stream)
+    out["prefill_append_q4_0_gqa32x8_d128_chunk2048_at14336"] = {
+        "ms_fused": round(ms_fused, 4), "ms_append_then_prefill": round(ms_two, 4),
+        "TFLOP/s_fused": round(w.flops() / (ms_fused * 1e-3) / 1e12, 2),
+        "frac_fused": round(w.flops() / (ms_fused * 1e-3) / 1e12 / peak, 4)}
+    del q, kn, vn, kc, vc, o, ws
     # the explicit (non-flash) path on the q4_0 16K chunk: dequant, S in f32, softmax, O = P V
     w = fa_inputs.WORKLOADS["prefill_q4_0_gqa32x8_d128_sq2048_sk16384_f16"]
     q, k, v = fa_inputs.make_qkv(w, device=dev, generate_on_device=True)
@@ -462,7 +494,8 @@ def other_legs(fa, dev, stream, flush, peaks):
     tf = w.flops() / (ms * 1e-3) / 1e12
     out["explicit_q4_0_gqa32x8_d128_sq2048_sk16384_f16"] = {
         "ms": round(ms, 4), "TFLOP/s": round(tf, 2), "frac": round(tf / peak, 4),
-        "note": "non-flash path: dequant, S in f32 (batched GEMM), softmax, O = P V (GEMM)"}
+        "note": "non-flash path: dequant, S in f32 (tcgen05 GEMM), softmax, O = P V (tcgen05 "
+                "GEMM)"}
     del q, kq, vq, o, ws
     # paged q4_0 decode: the 4 x 65536-key workload through 256-token pages in shuffled order,
     # and a batch of four different lengths
@@ -634,7 +667,8 @@ def run_reference(args, rank, world):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of the run; must equal WORLD_SIZE when launched by torchrun")
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -648,6 +682,9 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {world}: launch one process per GPU "
+                 "(torchrun --nproc-per-node N) for N > 1")
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:

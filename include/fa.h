@@ -122,6 +122,23 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B,
                     void* workspace, size_t workspace_bytes, int32_t* rescale_count,
                     fa_stream_t stream);
 
+/* fa_fwd_kv that also reports, per query row, the largest softmax numerator P it produced.
+ * The deferred rescale of "perf(rocm): defer SDPA accumulator rescale, stage Q once per block
+ * (#2306)" (What changed) keeps a row's frame f until a key block's maximum score exceeds it by
+ * more than 10 natural-log units, so every P = e^(s - f) the kernel writes stays at or below
+ * e^10 = 22026.47 (up to the rounding of the f32 exponent argument).  This call exposes that
+ * bound for testing.
+ *  p_max : optional device float [B, Hq, Sq] (NULL to skip): for every query row the largest P
+ *          value (before its rounding to the dtype) over all its key blocks, each relative to the
+ *          frame in force for that block; where the cut schedule splits a row between CTAs, the
+ *          largest over the pieces.  Not written when Sq == 1.
+ *  Other arguments, scratch, errors: as fa_fwd_kv (which is this call with p_max = NULL). */
+fa_status fa_fwd_kv_stats(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                          int Hkv, int Sq, int Sk, int kv_capacity, int D, int q_pos_offset,
+                          int causal, float scale, fa_dtype dtype, fa_kv_format k_format,
+                          fa_kv_format v_format, void* workspace, size_t workspace_bytes,
+                          int32_t* rescale_count, float* p_max, fa_stream_t stream);
+
 /* Scratch bytes fa_fwd_ex needs for this shape on the current device (decode: the split
  * partials; prefill: the partial rows of work units cut between CTAs, 0 when the launch runs
  * one unit per CTA). */
@@ -189,15 +206,18 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
                           fa_stream_t stream);
 
 /* The explicit (non-flash) attention path, for comparison with fa_fwd_kv: q4_0 sides are first
- * expanded to dense f16/bf16, S = scale * Q K^T is written out in f32 by a batched GEMM (cuBLAS),
- * a softmax kernel makes P (causal mask, rounded to the dtype), and O = P V is a second batched
- * GEMM.  Approach C of "FlashAttention on gfx90a: Why It's Broken and How to Fix It" (dequantize
- * K and V, two GEMMs and a softmax), the path that page measures against flash attention.
+ * expanded to dense f16/bf16, S = scale * Q K^T is written out in f32 by a batched GEMM, a
+ * softmax kernel makes P (causal mask, rounded to the dtype), and O = P V is a second batched
+ * GEMM -- Approach C of "FlashAttention on gfx90a: Why It's Broken and How to Fix It" (dequantize
+ * K and V, two GEMMs and a softmax), the path that page measures against flash attention.  Both
+ * GEMMs are this library's own tcgen05 kernel; S tiles that the causal mask hides from every row
+ * are not computed and the P V GEMM stops at each row tile's last visible key.
  *  Arguments: as fa_fwd_kv without a capacity (K, V: [B, Hkv, Sk, D] each, dense or q4_0).
  *  workspace: >= fa_explicit_workspace_bytes(...) bytes: S (4 bytes per score), P (2 bytes per
- *             score) and, per q4_0 side, its dense copy -- B*Hq*Sq*Sk*6 bytes and more, so this
- *             path is for moderate shapes (Hq = 32, Sq = 2048, Sk = 16384 needs 6.4 GB).
- *  Errors: as fa_fwd_ex; a failing cuBLAS call gives FA_ERR_CUDA. */
+ *             score), rows padded to a multiple of 64 keys, and per q4_0 side its dense copy --
+ *             about B*Hq*Sq*Sk*6 bytes, so this path is for moderate shapes (Hq = 32,
+ *             Sq = 2048, Sk = 16384 needs 6.4 GB).
+ *  Errors: as fa_fwd_ex; a tensor map the driver cannot encode gives FA_ERR_CUDA. */
 size_t fa_explicit_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D,
                                    fa_kv_format k_format, fa_kv_format v_format);
 fa_status fa_fwd_explicit(const void* q, const void* k, const void* v, void* o, int B, int Hq,
@@ -229,6 +249,37 @@ fa_status fa_quantize_q4_0(const void* x, void* out_q4, int B, int H, int S, int
 fa_status fa_append_q4_0(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                          int B, int H, int S_new, int kv_capacity, int pos0, int D,
                          fa_dtype dtype, fa_stream_t stream);
+
+/* Chunked prefill over q4_0 caches that appends the chunk to the caches in the same launch.
+ * The step before the fused path of "FlashAttention on gfx90a: Why It's Broken and How to Fix
+ * It" (Impact of the V Dequant Patch: the K/V cache is stored quantized, -ctk q4_0 -ctv q4_0):
+ * the chunk's own K and V are quantized into the caches and the chunk's queries attend to the
+ * whole cache, its own tokens included, as stored.
+ *  q, o           : [B, Hq, S_new, D] in `dtype`; query row i sits at position pos0 + i
+ *  k_new, v_new   : [B, Hkv, S_new, D] in `dtype`, the chunk's keys and values (finite)
+ *  k_cache,
+ *  v_cache        : q4_0 tensors built for [B, Hkv, kv_capacity, D]; tokens 0 .. pos0 - 1 hold
+ *                   the earlier chunks; tokens pos0 .. pos0 + S_new - 1 are overwritten with the
+ *                   bits fa_append_q4_0 writes; tokens past pos0 + S_new are untouched
+ *  Result: exactly fa_append_q4_0(k_new, v_new, ...) followed by fa_fwd_kv(q, k_cache,
+ *  v_cache, o, ..., Sk = pos0 + S_new, q_pos_offset = pos0, causal = 1, both formats q4_0).
+ *  Requires 0 <= pos0, pos0 + S_new <= kv_capacity, D in {64, 128}, and the shape checks of
+ *  fa_fwd.  workspace: >= fa_prefill_append_workspace_bytes(...) bytes, contents on entry
+ *  irrelevant (see fa_fwd_ex); the call also clears a small region of it with
+ *  cudaMemsetAsync on `stream`.
+ *  How it runs: at D = 128 one cooperative launch of the cut-schedule prefill, one CTA per SM:
+ *  every CTA first quantizes its share of the chunk (per (batch, kv head, 128-token cache
+ *  block)) and publishes it with a flag; a CTA's loads of a cache block holding chunk tokens
+ *  wait for that block's flag.  Other shapes (D = 64, or work too large for one CTA per SM's
+ *  segment table) run the append and the prefill as two launches on `stream`, with the same
+ *  result. */
+size_t fa_prefill_append_workspace_bytes(int B, int Hq, int Hkv, int S_new, int kv_capacity,
+                                         int D, int pos0);
+fa_status fa_prefill_append_q4_0(const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, void* o, int B, int Hq, int Hkv,
+                                 int S_new, int kv_capacity, int D, int pos0, float scale,
+                                 fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                 fa_stream_t stream);
 
 /* Synchronize `stream`, then report (and clear) any device-side error recorded by this
  * library's kernels since the last call: FA_ERR_TIMEOUT when a bounded wait inside a kernel ran
@@ -298,7 +349,7 @@ int64_t fa_decode_schedule(const int32_t* seq_lens, int B, int Hkv, int Sk, int 
                            int num_sms, int32_t* rows, int64_t max_rows);
 
 /* Library ABI version (major * 100 + minor): 101 adds fa_fwd_kv and fa_append_q4_0, 102
- * fa_decode_paged, 103 fa_fwd_explicit, 104 fa_prefill_schedule, 105 fa_decode_schedule. */
+ * fa_decode_paged, 103 fa_fwd_explicit, 104 fa_prefill_schedule, 105 fa_decode_schedule, 106 fa_fwd_kv_stats, 107 fa_prefill_append_q4_0. */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -28,7 +28,8 @@ EXPORTED = (
     "fa_quantize_q4_0", "fa_get_status", "fa_status_string", "fa_debug_wait_timeout",
     "fa_version", "fa_fwd_decode_noalloc", "fa_fwd_kv", "fa_append_q4_0", "fa_decode_paged",
     "fa_decode_paged_workspace_bytes", "fa_fwd_explicit", "fa_explicit_workspace_bytes",
-    "fa_prefill_schedule", "fa_decode_schedule",
+    "fa_prefill_schedule", "fa_decode_schedule", "fa_fwd_kv_stats",
+    "fa_prefill_append_workspace_bytes", "fa_prefill_append_q4_0",
 )
 
 _lib = None
@@ -89,8 +90,16 @@ def load_from(p: str) -> ctypes.CDLL:
     lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, i, vp, sz, vp,
                               vp]
     lib.fa_fwd_kv.restype = i
+    lib.fa_fwd_kv_stats.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, i, i, vp, sz,
+                                    vp, vp, vp]
+    lib.fa_fwd_kv_stats.restype = i
     lib.fa_append_q4_0.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.fa_append_q4_0.restype = i
+    lib.fa_prefill_append_workspace_bytes.argtypes = [i] * 7
+    lib.fa_prefill_append_workspace_bytes.restype = sz
+    lib.fa_prefill_append_q4_0.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp,
+                                           sz, vp]
+    lib.fa_prefill_append_q4_0.restype = i
     lib.fa_decode_paged_workspace_bytes.argtypes = [i] * 6
     lib.fa_decode_paged_workspace_bytes.restype = sz
     lib.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, i, vp,
@@ -399,10 +408,11 @@ def _side(t):
 def fa_fwd_kv(q, k, v, o=None, *, Sk: int | None = None, causal: bool = True,
               q_pos_offset: int | None = None, scale: float | None = None,
               workspace: torch.Tensor | None = None, rescale_count: torch.Tensor | None = None,
-              stream=None) -> torch.Tensor:
+              p_max: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Attention over K/V caches whose formats are chosen independently (each a dense tensor in
     q's dtype or a Q4Tensor) and whose token capacity (their third dimension) may exceed the Sk
-    tokens filled (default: the capacity).  q_pos_offset defaults to Sk - Sq."""
+    tokens filled (default: the capacity).  q_pos_offset defaults to Sk - Sq.  With p_max (f32
+    [B, Hq, Sq]) the call goes through fa_fwd_kv_stats, which writes each row's largest P."""
     if o is None:
         o = torch.empty_like(q)
     if q.dim() != 4 or not q.is_contiguous() or not o.is_contiguous() or o.shape != q.shape:
@@ -422,7 +432,7 @@ def fa_fwd_kv(q, k, v, o=None, *, Sk: int | None = None, causal: bool = True,
         q_pos_offset = Sk - Sq
     if scale is None:
         scale = D ** -0.5
-    _on_device(q, k, v, o, workspace, rescale_count)
+    _on_device(q, k, v, o, workspace, rescale_count, p_max)
     lib = load()
     if workspace is None:
         need = lib.fa_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, int(q_pos_offset), int(bool(causal)))
@@ -435,11 +445,23 @@ def fa_fwd_kv(q, k, v, o=None, *, Sk: int | None = None, causal: bool = True,
         if rescale_count.dtype != torch.int32 or rescale_count.numel() != B * Hq * Sq:
             raise ValueError("rescale_count must be int32 [B, Hq, Sq]")
         rc_ptr = rescale_count.data_ptr()
-    _check(lib.fa_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq,
-                         Sk, Scap, D, int(q_pos_offset), int(bool(causal)), float(scale),
-                         _dtype_code(q.dtype), kf, vf, ws_ptr, ws_bytes, rc_ptr, _stream(stream)),
-           "fa_fwd_kv")
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Sk, Scap, D,
+            int(q_pos_offset), int(bool(causal)), float(scale), _dtype_code(q.dtype), kf, vf,
+            ws_ptr, ws_bytes, rc_ptr)
+    if p_max is None:
+        _check(lib.fa_fwd_kv(*args, _stream(stream)), "fa_fwd_kv")
+    else:
+        if (p_max.dtype != torch.float32 or p_max.numel() != B * Hq * Sq
+                or not p_max.is_contiguous()):
+            raise ValueError("p_max must be a contiguous float32 [B, Hq, Sq] tensor")
+        _check(lib.fa_fwd_kv_stats(*args, p_max.data_ptr(), _stream(stream)), "fa_fwd_kv_stats")
     return o
+
+
+def fa_fwd_kv_stats(q, k, v, o=None, *, p_max: torch.Tensor, **kw) -> torch.Tensor:
+    """fa_fwd_kv that also writes, per query row, the largest softmax numerator P it produced
+    (p_max: f32 [B, Hq, Sq]; see fa.h)."""
+    return fa_fwd_kv(q, k, v, o, p_max=p_max, **kw)
 
 
 def q4_0_cache(B: int, H: int, capacity: int, D: int, device="cuda") -> Q4Tensor:
@@ -475,6 +497,51 @@ def fa_append_q4_0(k_new: torch.Tensor, k_cache: Q4Tensor, pos0: int,
                                  v_cache.data_ptr() if v_cache is not None else None, B, H, S_new,
                                  k_cache.S, int(pos0), D, _dtype_code(k_new.dtype),
                                  _stream(stream)), "fa_append_q4_0")
+
+
+def fa_prefill_append_workspace_bytes(B: int, Hq: int, Hkv: int, S_new: int, kv_capacity: int,
+                                      D: int, pos0: int) -> int:
+    return int(load().fa_prefill_append_workspace_bytes(B, Hq, Hkv, S_new, kv_capacity, D, pos0))
+
+
+def fa_prefill_append_q4_0(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                           k_cache: Q4Tensor, v_cache: Q4Tensor, pos0: int,
+                           o: torch.Tensor | None = None, *, scale: float | None = None,
+                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Append a chunk (k_new, v_new [B, Hkv, S_new, D]) to q4_0 caches at pos0 and run the
+    chunk's causal prefill (q [B, Hq, S_new, D] at positions pos0 ..) over the whole cache, in
+    one launch where the shape allows (see fa.h)."""
+    if o is None:
+        o = torch.empty_like(q)
+    if q.dim() != 4 or not q.is_contiguous() or not o.is_contiguous() or o.shape != q.shape:
+        raise ValueError("q and o must be contiguous [B, Hq, S_new, D] tensors of the same shape")
+    B, Hq, S_new, D = q.shape
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if t.dim() != 4 or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous [B, Hkv, S_new, D] tensor of q's dtype")
+    Bk, Hkv, Sn, Dk = k_new.shape
+    if (Bk, Sn, Dk) != (B, S_new, D) or tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError("k_new / v_new do not match q")
+    _check_q4(k_cache, "k_cache")
+    _check_q4(v_cache, "v_cache")
+    if k_cache.shape != v_cache.shape or (k_cache.B, k_cache.H, k_cache.D) != (B, Hkv, D):
+        raise ValueError("the caches must be [B, Hkv, capacity, D] q4_0 tensors")
+    if scale is None:
+        scale = D ** -0.5
+    _on_device(q, k_new, v_new, k_cache, v_cache, o, workspace)
+    lib = load()
+    if workspace is None:
+        need = lib.fa_prefill_append_workspace_bytes(B, Hq, Hkv, S_new, k_cache.S, D, int(pos0))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.fa_prefill_append_q4_0(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                      k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(), B, Hq,
+                                      Hkv, S_new, k_cache.S, D, int(pos0), float(scale),
+                                      _dtype_code(q.dtype), ws_ptr, ws_bytes, _stream(stream)),
+           "fa_prefill_append_q4_0")
+    return o
 
 
 def fa_decode_paged(q, k_pages, v_pages, block_table: torch.Tensor, seq_lens: torch.Tensor,

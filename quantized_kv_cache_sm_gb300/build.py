@@ -79,7 +79,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
                                                                       os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-lcublas",
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", f"-rpath={cuda_lib_dir(nvcc)}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

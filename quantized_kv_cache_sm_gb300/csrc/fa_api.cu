@@ -148,6 +148,13 @@ size_t workspace_any(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q_pos_of
 }
 
 }  // namespace
+
+bool encode_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                   uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1,
+                   CUtensorMapSwizzle sw) {
+  return make_map(m, base, dt, esize, d0, d1, d2, box0, box1, sw);
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -208,11 +215,11 @@ fa_status fa_append_q4_0(const void* k_new, const void* v_new, void* k_cache, vo
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
-                    int Sq, int Sk, int kv_capacity, int D, int q_pos_offset, int causal,
-                    float scale, fa_dtype dtype, fa_kv_format k_format, fa_kv_format v_format,
-                    void* workspace, size_t workspace_bytes, int32_t* rescale_count,
-                    fa_stream_t stream) {
+fa_status fa_fwd_kv_stats(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                          int Hkv, int Sq, int Sk, int kv_capacity, int D, int q_pos_offset,
+                          int causal, float scale, fa_dtype dtype, fa_kv_format k_format,
+                          fa_kv_format v_format, void* workspace, size_t workspace_bytes,
+                          int32_t* rescale_count, float* p_max, fa_stream_t stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, Hq, Hkv, Sq, Sk, D, q_pos_offset, causal, scale, dtype, k_format);
   if (st != FA_OK) return st;
@@ -276,6 +283,7 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B,
   L.v_scale = vq4 ? static_cast<const uint8_t*>(v) + kv_scale_off : nullptr;
   L.o = o;
   L.rescale_count = rescale_count;
+  L.p_max = p_max;
   L.B = B;
   L.Hq = Hq;
   L.Hkv = Hkv;
@@ -294,6 +302,106 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B,
   L.tag = next_call_tag();
   L.num_sms = num_sms();
   return prefill_launch(L, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                    int Sq, int Sk, int kv_capacity, int D, int q_pos_offset, int causal,
+                    float scale, fa_dtype dtype, fa_kv_format k_format, fa_kv_format v_format,
+                    void* workspace, size_t workspace_bytes, int32_t* rescale_count,
+                    fa_stream_t stream) {
+  return fa_fwd_kv_stats(q, k, v, o, B, Hq, Hkv, Sq, Sk, kv_capacity, D, q_pos_offset, causal,
+                         scale, dtype, k_format, v_format, workspace, workspace_bytes,
+                         rescale_count, nullptr, stream);
+}
+
+// the fused append's argument checks (0: fine), shared by the call and its scratch query
+static fa_status append_checks(int B, int Hq, int Hkv, int S_new, int kv_capacity, int D,
+                               int pos0) {
+  if (pos0 < 0 || S_new < 1 || static_cast<int64_t>(pos0) + S_new > kv_capacity)
+    return FA_ERR_INVALID_ARG;
+  const fa_status st = check_common(B, Hq, Hkv, S_new, pos0 + S_new, D, pos0, 1, 1.f, FA_F16,
+                                    FA_KV_Q4_0);
+  if (st != FA_OK) return st;
+  if (static_cast<int64_t>(B) * Hkv * kv_capacity * D >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t fa_prefill_append_workspace_bytes(int B, int Hq, int Hkv, int S_new, int kv_capacity,
+                                         int D, int pos0) {
+  if (append_checks(B, Hq, Hkv, S_new, kv_capacity, D, pos0) != FA_OK) return 0;
+  const size_t fused = prefill_append_workspace_bytes(B, Hq, Hkv, S_new, pos0 + S_new, pos0, D,
+                                                      num_sms());
+  if (fused > 0) return fused;
+  // shapes that run as an append followed by the prefill: the prefill's own scratch
+  return workspace_for(B, Hq, Hkv, S_new, pos0 + S_new, D, pos0, 1, true, true, nullptr,
+                       nullptr);
+}
+
+fa_status fa_prefill_append_q4_0(const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, void* o, int B, int Hq, int Hkv,
+                                 int S_new, int kv_capacity, int D, int pos0, float scale,
+                                 fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                 fa_stream_t stream) {
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(o))
+    return FA_ERR_INVALID_ARG;
+  fa_status st = append_checks(B, Hq, Hkv, S_new, kv_capacity, D, pos0);
+  if (st != FA_OK) return st;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  const int Sk = pos0 + S_new;
+  const size_t need = fa_prefill_append_workspace_bytes(B, Hq, Hkv, S_new, kv_capacity, D, pos0);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return FA_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == FA_BF16;
+  const size_t soff = q4_scale_offset(static_cast<int64_t>(B) * Hkv * kv_capacity, D);
+  const int nsm = num_sms();
+  if (prefill_append_workspace_bytes(B, Hq, Hkv, S_new, Sk, pos0, D, nsm) > 0) {
+    const CUtensorMapDataType tdt =
+        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t BHkv = static_cast<uint64_t>(B) * Hkv;
+    PrefillLaunch L{};
+    if (!make_map(&L.tm_q, q, tdt, 2, D, S_new, static_cast<uint64_t>(B) * Hq, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !kv_map(&L.tm_k, k_cache, true, tdt, D, kv_capacity, BHkv, 128,
+                CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !kv_map(&L.tm_v, v_cache, true, tdt, D, kv_capacity, BHkv, 128,
+                CU_TENSOR_MAP_SWIZZLE_64B))
+      return FA_ERR_CUDA;
+    uint8_t* kc = static_cast<uint8_t*>(k_cache);
+    uint8_t* vc = static_cast<uint8_t*>(v_cache);
+    L.k_scale = kc + soff;
+    L.v_scale = vc + soff;
+    L.o = o;
+    L.B = B;
+    L.Hq = Hq;
+    L.Hkv = Hkv;
+    L.Sq = S_new;
+    L.Sk = Sk;
+    L.Scap = kv_capacity;
+    L.D = D;
+    L.q_pos_offset = pos0;
+    L.causal = 1;
+    L.scale = scale;
+    L.bf16 = bf16;
+    L.kq4 = L.vq4 = true;
+    L.workspace = workspace;
+    L.workspace_bytes = workspace_bytes;
+    L.tag = next_call_tag();
+    L.num_sms = nsm;
+    const PrefillAppend A = {k_new, v_new, kc, vc, kc + soff, vc + soff, pos0, S_new};
+    const cudaError_t e = prefill_append_launch(L, A, s);
+    if (e == cudaSuccess) return FA_OK;
+    if (e != cudaErrorNotSupported) return FA_ERR_CUDA;
+    (void)cudaGetLastError();
+  }
+  // not fusable (D = 64, or a cut that does not fit): append, then the prefill over the cache
+  st = fa_append_q4_0(k_new, v_new, k_cache, v_cache, B, Hkv, S_new, kv_capacity, pos0, D, dtype,
+                      stream);
+  if (st != FA_OK) return st;
+  return fa_fwd_kv(q, k_cache, v_cache, o, B, Hq, Hkv, S_new, Sk, kv_capacity, D, pos0, 1, scale,
+                   dtype, FA_KV_Q4_0, FA_KV_Q4_0, workspace, workspace_bytes, nullptr, stream);
 }
 
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
@@ -438,10 +546,10 @@ fa_status fa_fwd_explicit(const void* q, const void* k, const void* v, void* o, 
   L.bf16 = dtype == FA_BF16;
   L.kq4 = kq4;
   L.vq4 = vq4;
-  int cublas_status = 0;
-  if (explicit_launch(L, reinterpret_cast<cudaStream_t>(stream), &cublas_status) != cudaSuccess)
+  int map_status = 0;
+  if (explicit_launch(L, reinterpret_cast<cudaStream_t>(stream), &map_status) != cudaSuccess)
     return FA_ERR_CUDA;
-  return cublas_status ? FA_ERR_CUDA : FA_OK;
+  return map_status ? FA_ERR_CUDA : FA_OK;
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
@@ -474,15 +582,16 @@ fa_status fa_get_status(fa_stream_t stream) {
   if (e != cudaSuccess) return FA_ERR_CUDA;
   const uint32_t a = prefill_take_error();
   const uint32_t b = decode_take_error();
+  const uint32_t x = explicit_take_error();
   uint32_t c = 0;
   if (cudaMemcpyFromSymbol(&c, g_debug_error, sizeof(c)) != cudaSuccess) return FA_ERR_CUDA;
   const uint32_t z = 0;
   if (c != 0 && cudaMemcpyToSymbol(g_debug_error, &z, sizeof(z)) != cudaSuccess)
     return FA_ERR_CUDA;
-  if (a == 0xffffffffu || b == 0xffffffffu) return FA_ERR_CUDA;
+  if (a == 0xffffffffu || b == 0xffffffffu || x == 0xffffffffu) return FA_ERR_CUDA;
   if (b == kErrBadIndex) return FA_ERR_INVALID_ARG;
   if (a == kErrSchedule) return FA_ERR_UNSUPPORTED;
-  if (a || b || c) return FA_ERR_TIMEOUT;
+  if (a || b || c || x) return FA_ERR_TIMEOUT;
   return FA_OK;
 }
 
@@ -538,6 +647,6 @@ int64_t fa_decode_schedule(const int32_t* seq_lens, int B, int Hkv, int Sk, int 
   return decode_debug_schedule(seq_lens, B, Hkv, Sk, cap, kq4, vq4, num_sms, rows, max_rows);
 }
 
-int fa_version(void) { return 105; }
+int fa_version(void) { return 107; }
 
 }  // extern "C"

@@ -5,20 +5,30 @@
 // "FlashAttention on gfx90a: Why It's Broken and How to Fix It" (Approach C: dequantize K and V
 // to f16, then two GEMMs and a softmax) and the "explicit f32 matmul + softmax + matmul"
 // reference of "perf(rocm): defer SDPA accumulator rescale, stage Q once per block (#2306)" (Test
-// plan).  The two GEMMs are plain library GEMMs (cuBLAS); the dequant and softmax are kernels
-// of this file.
+// plan).  Every step runs in kernels of this file; both GEMMs are one tcgen05 kernel.
 //
 // Grouped-query heads: the G = Hq / Hkv query heads of a kv head are consecutive rows of Q, so
 // one GEMM per (batch, kv head) computes their scores against that kv head's keys at once:
 // S_g [G*Sq, Sk] = Q_g [G*Sq, D] K^T [D, Sk]; O_g [G*Sq, D] = P_g [G*Sq, Sk] V [Sk, D].
-#include <cublas_v2.h>
-
-#include <mutex>
-
+// S and P rows are padded to Skp = Sk rounded up to 64 (the GEMM's K step), so that every row of
+// P starts on a 16-byte boundary for the tensor-memory-access loads; the padding of P is zero.
+//
+// The GEMM (gemm_kernel): one CTA computes a 128 x BN tile of C = alpha * A B for one group.
+// A [M, K] is K-major (Q, or P); B is K-major (K: [N = keys, K = D]) or MN-major (V: [K = keys,
+// N = D]).  Warp 0 streams 64-wide K slices of A and B into a ring of shared-memory stages by TMA
+// (128-byte swizzle), warp 1 issues tcgen05.mma (M 128, N = BN, K 16; f32 accumulator in tensor
+// memory), then all four warps read the accumulator back (one row per thread) and store it.
+// Causal masking is exact in the softmax kernel; the GEMMs only skip work that the mask makes
+// irrelevant: S tiles whose keys lie past every row's last visible key are not computed (the
+// softmax never reads them), and the P V GEMM stops its K loop at the tile's last visible key
+// (P is zero beyond it).
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
 namespace fa {
+
+__device__ uint32_t g_explicit_error;
+
 namespace {
 
 template <bool BF16>
@@ -58,16 +68,17 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
 }
 
 // One CTA per row of S (row r of group (b, hkv): query head hkv*G + r / Sq, query i = r % Sq):
-// keys j > q_pos_offset + i are masked when causal; P = e^(s - max) / sum, rounded to the dtype.
+// keys j > q_pos_offset + i are masked when causal; P = e^(s - max) / sum, rounded to the dtype;
+// P is zero at masked keys and in the row padding [Sk, Skp).
 template <bool BF16>
 __global__ void __launch_bounds__(256) softmax_kernel(const float* __restrict__ S,
                                                       uint16_t* __restrict__ P, int Sq, int Sk,
-                                                      int q_pos_offset, int causal) {
+                                                      int Skp, int q_pos_offset, int causal) {
   const int64_t row = blockIdx.x;
   const int i = static_cast<int>(row % Sq);
   const int lim = causal ? min(Sk, q_pos_offset + i + 1) : Sk;  // visible keys [0, lim)
-  const float* s = S + row * Sk;
-  uint16_t* p = P + row * Sk;
+  const float* s = S + row * Skp;
+  uint16_t* p = P + row * Skp;
   __shared__ float red[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float m = -INFINITY;
@@ -90,42 +101,245 @@ __global__ void __launch_bounds__(256) softmax_kernel(const float* __restrict__ 
 #pragma unroll
   for (int w = 0; w < 8; ++w) l += red[w];
   const float inv = 1.f / l;
-  for (int j = tid; j < Sk; j += 256) p[j] = to_bits<BF16>(j < lim ? __expf(s[j] - m) * inv : 0.f);
+  for (int j = tid; j < Skp; j += 256) p[j] = to_bits<BF16>(j < lim ? __expf(s[j] - m) * inv : 0.f);
 }
 
-// one cuBLAS handle per device, created on first use (the library never destroys it)
-cublasHandle_t handle_for_current_device() {
-  static std::mutex mu;
-  static cublasHandle_t handles[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> g(mu);
-  if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
-  return handles[dev];
+// ------------------------------------------------------------------------------------------
+// tcgen05 GEMM
+// ------------------------------------------------------------------------------------------
+constexpr int kGM = 128;      // rows of a C tile (the MMA's M)
+constexpr int kGK = 64;       // K slice per stage: one 128-byte swizzle atom of 16-bit values
+constexpr int kGStages = 3;   // 3 x 32 KB: two CTAs fit on an SM
+constexpr int kGThreads = 128;
+
+template <int BN>
+struct GCfg {
+  static constexpr int kABytes = kGM * kGK * 2;       // 16 KB
+  static constexpr int kBBytes = BN * kGK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kOffBar = kGStages * kStageBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, slots, alignment slack
+  static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+};
+
+struct GemmArgs {
+  void* c;              // C [groups][M][ldc]: f32 (S) or 16-bit (O)
+  int64_t ldc;          // elements per row of C
+  int64_t c_group;      // elements per group of C
+  int M, N, K;          // per group; N: columns of C written (S: Skp; O: D)
+  float alpha;
+  // causal skipping: C row r of a group is query i = r % Sq, whose last visible key is
+  // q_pos_offset + i (non-causal: all keys)
+  int Sq, q_pos_offset, causal;
+  int k_is_keys;        // 1: the K dimension runs over keys (P V), 0: the N dimension does (Q K^T)
+};
+
+// largest query index among C rows [m0, m0 + 128) of a group
+__device__ __forceinline__ int tile_i_max(const GemmArgs& a, int m0) {
+  const int m_last = min(m0 + kGM, a.M) - 1;
+  // the tile lies within one head's rows unless it crosses a multiple of Sq
+  if (m0 / a.Sq == m_last / a.Sq) return m_last % a.Sq;
+  return a.Sq - 1;
 }
+
+template <int BN, bool BF16, bool B_MN, bool OUT_F32>
+__global__ void __launch_bounds__(kGThreads) gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                                                         const __grid_constant__ CUtensorMap tm_b,
+                                                         const GemmArgs args) {
+  using C = GCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto full = [&](int s) -> uint32_t { return bar0 + 8u * s; };
+  auto empty = [&](int s) -> uint32_t { return bar0 + 8u * (kGStages + s); };
+  const uint32_t acc_full = bar0 + 8u * (2 * kGStages);
+  const uint32_t drain = bar0 + 8u * (2 * kGStages + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::kOffBar + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffBar + 136);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = static_cast<int>(blockIdx.x) * BN;
+  const int m0 = static_cast<int>(blockIdx.y) * kGM;
+  const int grp = static_cast<int>(blockIdx.z);
+
+  // the work the causal mask leaves for this tile (uniform over the CTA: decided before any
+  // barrier or tensor-memory allocation)
+  int k_end = args.K;
+  if (args.causal) {
+    const int last_key = args.q_pos_offset + tile_i_max(args, m0);
+    if (args.k_is_keys)
+      k_end = min(args.K, last_key + 1);
+    else if (n0 > last_key)
+      return;  // every score of this tile is masked: the softmax never reads it
+  }
+  const int nk = (k_end + kGK - 1) / kGK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_b);
+    int issued = 0;
+    for (int kb = 0; kb < nk && ok; ++kb) {
+      const int s = kb % kGStages;
+      if (kb >= kGStages)
+        ok = mbar_wait(empty(s), ((kb / kGStages) - 1) & 1, abort_flag, &g_explicit_error);
+      if (!ok) break;
+      ++issued;
+      const uint32_t a_dst = sbase + s * C::kStageBytes;
+      const uint32_t b_dst = a_dst + C::kABytes;
+      mbar_arrive_expect_tx(full(s), C::kStageBytes);
+      tma_load_3d(a_dst, &tm_a, full(s), kb * kGK, m0, grp);
+      if (B_MN) {
+        // [K rows = keys][N = BN columns] as BN/64 boxes of 64 columns x 64 keys
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c)
+          tma_load_3d(b_dst + c * (kGK * 128), &tm_b, full(s), n0 + c * 64, kb * kGK, grp);
+      } else {
+        tma_load_3d(b_dst, &tm_b, full(s), kb * kGK, n0, grp);
+      }
+    }
+    if (!ok) {
+      // let the copies already issued land before shared memory goes away
+      volatile int never = 0;
+      for (int kb = max(0, issued - kGStages); kb < issued; ++kb)
+        mbar_wait(full(kb % kGStages), (kb / kGStages) & 1, &never, nullptr, kWaitLimitNs);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = make_idesc_f16(kGM, BN, BF16, B_MN);
+    for (int kb = 0; kb < nk && ok; ++kb) {
+      const int s = kb % kGStages;
+      ok = mbar_wait(full(s), (kb / kGStages) & 1, abort_flag, &g_explicit_error);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a_s = sbase + s * C::kStageBytes;
+      const uint32_t b_s = a_s + C::kABytes;
+#pragma unroll
+      for (int kk = 0; kk < kGK / 16; ++kk) {
+        const uint64_t ad = make_sdesc_sw128(a_s + kk * 32, 16, 1024);
+        const uint64_t bd = B_MN ? make_sdesc_sw128(b_s + kk * (16 * 128), kGK * 128, 1024)
+                                 : make_sdesc_sw128(b_s + kk * 32, 16, 1024);
+        mma_ss(tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(empty(s));
+    }
+    if (ok) {
+      mma_commit(acc_full);
+    } else {
+      volatile int never = 0;
+      mma_commit(drain);
+      mbar_wait(drain, 0, &never, nullptr, kWaitLimitNs);
+    }
+  }
+  __syncwarp();
+
+  // ---------------------------------------------------------------- epilogue, all four warps
+  ok = !*abort_flag && mbar_wait(acc_full, 0, abort_flag, &g_explicit_error);
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok) {
+    tc_fence_after();
+    const int row = m0 + 32 * warp + lane;
+    const bool store = row < args.M;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c0, r);
+      tmem_wait_ld();
+      reg_fence32(r);
+      if (!store || n0 + c0 >= args.N) continue;
+      if (OUT_F32) {
+        float* dst = static_cast<float*>(args.c) + grp * args.c_group + row * args.ldc + n0 + c0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<float4*>(dst)[i] =
+              make_float4(__uint_as_float(r[4 * i]) * args.alpha,
+                          __uint_as_float(r[4 * i + 1]) * args.alpha,
+                          __uint_as_float(r[4 * i + 2]) * args.alpha,
+                          __uint_as_float(r[4 * i + 3]) * args.alpha);
+      } else {
+        uint16_t* dst =
+            static_cast<uint16_t*>(args.c) + grp * args.c_group + row * args.ldc + n0 + c0;
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * args.alpha,
+                              __uint_as_float(r[2 * i + 1]) * args.alpha);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<uint4*>(dst)[i] =
+              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int BN, bool BF16, bool B_MN, bool OUT_F32>
+cudaError_t gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                        int groups, cudaStream_t stream) {
+  using C = GCfg<BN>;
+  auto kern = gemm_kernel<BN, BF16, B_MN, OUT_F32>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((a.N + BN - 1) / BN, (a.M + kGM - 1) / kGM, groups);
+  kern<<<grid, kGThreads, C::kSmemBytes, stream>>>(ta, tb, a);
+  return cudaGetLastError();
+}
+
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+int padded_keys(int Sk) { return (Sk + kGK - 1) / kGK * kGK; }
 
 }  // namespace
 
 size_t explicit_workspace(int B, int Hq, int Hkv, int Sq, int Sk, int D, bool kq4, bool vq4) {
-  auto al = [](size_t n) { return (n + 255) / 256 * 256; };
   const size_t rows = static_cast<size_t>(B) * Hq * Sq;
-  size_t n = al(rows * Sk * sizeof(float)) + al(rows * Sk * 2);  // S (f32), P (dtype)
+  const size_t skp = static_cast<size_t>(padded_keys(Sk));
+  size_t n = align256(rows * skp * sizeof(float)) + align256(rows * skp * 2);  // S (f32), P
   const size_t kv = static_cast<size_t>(B) * Hkv * Sk * D * 2;
-  if (kq4) n += al(kv);
-  if (vq4) n += al(kv);
+  if (kq4) n += align256(kv);
+  if (vq4) n += align256(kv);
   return n;
 }
 
-cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* cublas_status) {
-  *cublas_status = 0;
-  auto al = [](size_t n) { return (n + 255) / 256 * 256; };
+cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* map_status) {
+  *map_status = 0;
   const int G = L.Hq / L.Hkv;
+  const int Skp = padded_keys(L.Sk);
   const size_t rows = static_cast<size_t>(L.B) * L.Hq * L.Sq;
   uint8_t* ws = static_cast<uint8_t*>(L.workspace);
   float* S = reinterpret_cast<float*>(ws);
-  ws += al(rows * L.Sk * sizeof(float));
+  ws += align256(rows * Skp * sizeof(float));
   uint16_t* P = reinterpret_cast<uint16_t*>(ws);
-  ws += al(rows * L.Sk * 2);
+  ws += align256(rows * Skp * 2);
   const size_t kv = static_cast<size_t>(L.B) * L.Hkv * L.Sk * L.D;
   const int64_t nblocks = static_cast<int64_t>(kv / 32);
   const unsigned dq_grid = static_cast<unsigned>((nblocks + 255) / 256);
@@ -141,56 +355,80 @@ cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* c
   };
   if (L.kq4) {
     uint16_t* kd = reinterpret_cast<uint16_t*>(ws);
-    ws += al(kv * 2);
+    ws += align256(kv * 2);
     dequant(L.k, kd);
     K = kd;
   }
   if (L.vq4) {
     uint16_t* vd = reinterpret_cast<uint16_t*>(ws);
-    ws += al(kv * 2);
+    ws += align256(kv * 2);
     dequant(L.v, vd);
     V = vd;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  cublasHandle_t h = handle_for_current_device();
-  if (!h) {
-    *cublas_status = 1;
-    return cudaSuccess;
-  }
-  const cudaDataType_t dt = L.bf16 ? CUDA_R_16BF : CUDA_R_16F;
+
   const int M = G * L.Sq;  // rows of a (batch, kv head) group
-  const int batch = L.B * L.Hkv;
-  cublasStatus_t st = cublasSetStream(h, stream);
-  // S^T (col-major Sk x M) = K (Sk x D, from row-major K: op T) * Q_g^T (D x M)
-  const float alpha = L.scale, beta = 0.f;
-  if (st == CUBLAS_STATUS_SUCCESS)
-    st = cublasGemmStridedBatchedEx(
-        h, CUBLAS_OP_T, CUBLAS_OP_N, L.Sk, M, L.D, &alpha, K, dt, L.D,
-        static_cast<long long>(L.Sk) * L.D, L.q, dt, L.D, static_cast<long long>(M) * L.D, &beta,
-        S, CUDA_R_32F, L.Sk, static_cast<long long>(M) * L.Sk, batch, CUBLAS_COMPUTE_32F,
-        CUBLAS_GEMM_DEFAULT);
-  if (st != CUBLAS_STATUS_SUCCESS) {
-    *cublas_status = static_cast<int>(st);
+  const int groups = L.B * L.Hkv;
+  const CUtensorMapDataType tdt =
+      L.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  // S = scale Q_g K^T: A = Q_g [M][D], B = K [Sk][D] (K-major), C = S [M][Skp] f32; tiles of
+  // 128 keys, the last one covering the padding
+  CUtensorMap tq, tk, tp, tv;
+  if (!encode_map_3d(&tq, L.q, tdt, 2, L.D, M, groups, kGK, kGM, sw) ||
+      !encode_map_3d(&tk, K, tdt, 2, L.D, L.Sk, groups, kGK, 128, sw) ||
+      !encode_map_3d(&tp, P, tdt, 2, Skp, M, groups, kGK, kGM, sw) ||
+      !encode_map_3d(&tv, V, tdt, 2, L.D, L.Sk, groups, 64, kGK, sw)) {
+    *map_status = 1;
     return cudaSuccess;
   }
+  GemmArgs ga;
+  ga.c = S;
+  ga.ldc = Skp;
+  ga.c_group = static_cast<int64_t>(M) * Skp;
+  ga.M = M;
+  ga.N = Skp;
+  ga.K = L.D;
+  ga.alpha = L.scale;
+  ga.Sq = L.Sq;
+  ga.q_pos_offset = L.q_pos_offset;
+  ga.causal = L.causal;
+  ga.k_is_keys = 0;
+  e = L.bf16 ? gemm_launch<128, true, false, true>(tq, tk, ga, groups, stream)
+             : gemm_launch<128, false, false, true>(tq, tk, ga, groups, stream);
+  if (e != cudaSuccess) return e;
   if (L.bf16)
     softmax_kernel<true><<<static_cast<unsigned>(rows), 256, 0, stream>>>(
-        S, P, L.Sq, L.Sk, L.q_pos_offset, L.causal);
+        S, P, L.Sq, L.Sk, Skp, L.q_pos_offset, L.causal);
   else
     softmax_kernel<false><<<static_cast<unsigned>(rows), 256, 0, stream>>>(
-        S, P, L.Sq, L.Sk, L.q_pos_offset, L.causal);
+        S, P, L.Sq, L.Sk, Skp, L.q_pos_offset, L.causal);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // O^T (col-major D x M) = V^T (D x Sk, row-major V read as is) * P_g^T (Sk x M)
-  const float one = 1.f;
-  st = cublasGemmStridedBatchedEx(
-      h, CUBLAS_OP_N, CUBLAS_OP_N, L.D, M, L.Sk, &one, V, dt, L.D,
-      static_cast<long long>(L.Sk) * L.D, P, dt, L.Sk, static_cast<long long>(M) * L.Sk, &beta,
-      L.o, dt, L.D, static_cast<long long>(M) * L.D, batch, CUBLAS_COMPUTE_32F,
-      CUBLAS_GEMM_DEFAULT);
-  if (st != CUBLAS_STATUS_SUCCESS) *cublas_status = static_cast<int>(st);
-  return cudaSuccess;
+  // O_g = P_g V: A = P_g [M][Skp], B = V [Sk][D] (MN-major; keys past Sk read as zeros, where
+  // P is zero too), C = O_g [M][D] in the dtype
+  GemmArgs go = ga;
+  go.c = L.o;
+  go.ldc = L.D;
+  go.c_group = static_cast<int64_t>(M) * L.D;
+  go.N = L.D;
+  go.K = Skp;
+  go.alpha = 1.f;
+  go.k_is_keys = 1;
+  if (L.D == 128)
+    return L.bf16 ? gemm_launch<128, true, true, false>(tp, tv, go, groups, stream)
+                  : gemm_launch<128, false, true, false>(tp, tv, go, groups, stream);
+  return L.bf16 ? gemm_launch<64, true, true, false>(tp, tv, go, groups, stream)
+                : gemm_launch<64, false, true, false>(tp, tv, go, groups, stream);
+}
+
+uint32_t explicit_take_error() {
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_explicit_error, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  const uint32_t z = 0;
+  cudaMemcpyToSymbol(g_explicit_error, &z, sizeof(z));
+  return v;
 }
 
 }  // namespace fa

@@ -7,12 +7,19 @@
 
 namespace fa {
 
+// 3-D tiled TMA map over a contiguous [d2][d1][d0] tensor of esize-byte elements; box =
+// {box0, box1, 1}; false if the driver entry point is missing or rejects the arguments
+bool encode_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                   uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1,
+                   CUtensorMapSwizzle sw);
+
 struct PrefillLaunch {
   CUtensorMap tm_q, tm_k, tm_v;  // Q tiles; K and V: dense tiles or q4_0 nibble tiles
   void* o;
   const void* k_scale;           // scale plane of a q4_0 K (else null)
   const void* v_scale;           // scale plane of a q4_0 V (else null)
   int32_t* rescale_count;
+  float* p_max;                  // optional per-row largest P (see fa_fwd_kv_stats)
   int B, Hq, Hkv, Sq, Sk, Scap, D, q_pos_offset, causal;  // Scap: K/V tokens per (b, kv head)
   float scale;
   bool bf16, kq4, vq4;
@@ -24,6 +31,26 @@ struct PrefillLaunch {
   int num_sms;
 };
 cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream);
+// A chunk appended to q4_0 K and V caches by the prefill launch itself: k_new / v_new
+// [B, Hkv, len, D] in the dtype, quantized into tokens [pos0, pos0 + len) of the caches (nibble
+// and scale planes writable here) before the attention reads those tokens back.
+struct PrefillAppend {
+  const void* k_new;
+  const void* v_new;
+  void* k_nib;
+  void* v_nib;
+  void* k_sc;
+  void* v_sc;
+  int pos0, len;
+};
+// the fused append-and-prefill (L: q4_0 K and V, D = 128, causal, Sq = A.len, q_pos_offset =
+// A.pos0); cudaErrorNotSupported when the shape cannot run fused (the caller appends and then
+// runs the prefill), cudaErrorInvalidValue when the workspace is short
+cudaError_t prefill_append_launch(const PrefillLaunch& L, const PrefillAppend& A,
+                                  cudaStream_t stream);
+// its scratch (0: the shape cannot run fused)
+size_t prefill_append_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int q_pos_offset,
+                                      int D, int num_sms);
 // scratch the prefill launch needs to cut work units between CTAs (0: it runs whole units)
 size_t prefill_workspace_bytes(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causal,
                                int D, int num_sms);
@@ -99,8 +126,9 @@ struct ExplicitLaunch {
   bool bf16, kq4, vq4;
 };
 size_t explicit_workspace(int B, int Hq, int Hkv, int Sq, int Sk, int D, bool kq4, bool vq4);
-// returns the CUDA launch status; *cublas_status is non-zero when a cuBLAS call failed
-cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* cublas_status);
+// returns the CUDA launch status; *map_status is non-zero when a TMA map could not be encoded
+cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* map_status);
+uint32_t explicit_take_error();
 
 cudaError_t debug_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
 uint32_t debug_take_error();

@@ -31,8 +31,11 @@
 //   warps 2, 3   q4_0 dequant (q4_0 variant only; idle otherwise), two key rows per thread
 //   warps 4..7   softmax / rescale / epilogue of query tile A, one row per thread
 //   warps 8..11  the same for query tile B
+#include <algorithm>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_quant.cuh"
 
 namespace fa {
 
@@ -102,6 +105,7 @@ struct PrefillArgs {
   const uint8_t* k_scale;  // q4_0 only: fp16 scale planes [B, Hkv, Sk, D/32]
   const uint8_t* v_scale;
   int32_t* rescale_count;  // optional [B, Hq, Sq]
+  float* p_max;            // optional [B, Hq, Sq]: the largest P the row's softmax produced
   int B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, n_qtiles, n_pairs;
   int Scap;  // tokens per (batch, kv head) in the K/V tensors (row stride); Sk <= Scap
   float scale_log2;
@@ -112,6 +116,19 @@ struct PrefillArgs {
   float* part;           // partial rows of units cut between CTAs (workspace), 2 slots per CTA
   uint32_t* pflags;      // [n_ctas][2] publication flags (workspace), tagged per call
   uint32_t tag;
+  // a chunk appended to q4_0 K and V caches in the same launch (prefill_seg_kernel with q4_0
+  // on both sides, cooperative launch): phase 1 quantizes tokens [app_pos0, app_pos0 + app_len)
+  // of every (batch, kv head) from k_new / v_new into the caches, one item per (batch, kv head,
+  // 128-key cache block), and sets the item's flag in app_flags (zeroed before the launch);
+  // the producer waits for an item's flag before it reads that block from the caches
+  const uint16_t* k_new;  // [B, Hkv, app_len, D]
+  const uint16_t* v_new;
+  uint8_t* k_nib;         // the caches' nibble planes [B, Hkv, Scap, D/2]
+  uint8_t* v_nib;
+  __half* k_scw;          // the caches' scale planes [B, Hkv, Scap, D/32]
+  __half* v_scw;
+  uint32_t* app_flags;    // [B * Hkv * app_nb]; null: no append
+  int app_pos0, app_len, app_j_lo, app_nb;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -301,10 +318,16 @@ __device__ __forceinline__ float block_row_exp_regs(uint32_t scol, const float (
 // read is faster in the one-unit-per-CTA kernel and in the cut-schedule kernel with exactly
 // one q4_0 side (by 11 % with a q4_0 V), slower by 2 % in the dense cut-schedule kernel, even
 // with q4_0 on both sides.
+//
+// tmax tracks the base-2 exponent of the largest P written so far, t = s_max * sl2 - f taken
+// after the frame test (P is monotonic in the score, so the block's largest P is that of its
+// largest score; t is formed from the rounded s_max * sl2 the frame test uses, so it can differ
+// from the exponent of the stored P by an f32 rounding); the frame rule keeps t <= the margin,
+// so P <= e^10.
 template <int D, bool BF16, bool ONE_READ>
 __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool need_mask,
                                               int rel_lim, float sl2, bool o_live, float& f,
-                                              float& l, int& nres) {
+                                              float& l, int& nres, float& tmax) {
   auto rescale_o = [&](float alpha) {
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
@@ -334,6 +357,7 @@ __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool
       f = m2;
       ++nres;
     }
+    tmax = fmaxf(tmax, m2 - f);  // -inf for a fully masked row block; NaN (ignored) if also f
     l += block_row_exp_regs<BF16>(scol, s, sl2, -f);
     if (any && o_live) rescale_o(alpha);
   } else {
@@ -354,6 +378,7 @@ __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool
         tmem_wait_st();
       }
     }
+    tmax = fmaxf(tmax, m2 - f);  // -inf for a fully masked row block; NaN (ignored) if also f
     // pass 2: P = 2^(t - f) over the first half of S, row sum
     const float nf = -f;
     l += need_mask ? block_row_exp<true, BF16>(scol, rel_lim, sl2, nf)
@@ -610,6 +635,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
     float f = -INFINITY;  // frame, base-2 units of the scaled score
     float l = 0.f;
     int nres = 0;
+    float tmax = -INFINITY;  // log2 of the largest P written
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       ok = mbar_wait(bar(kBarSFull + t), j & 1, abort_flag, &g_prefill_error);
@@ -623,7 +649,8 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
       // last visible key of this row, relative to the block
       const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
-      softmax_block<D, BF16, true>(scol, ocol, need_mask, rel_lim, sl2, j > 0, f, l, nres);
+      softmax_block<D, BF16, true>(scol, ocol, need_mask, rel_lim, sl2, j > 0, f, l, nres,
+                                   tmax);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPReady + t));
@@ -659,6 +686,8 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       }
       if (store && args.rescale_count)
         args.rescale_count[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = nres;
+      if (store && args.p_max)
+        args.p_max[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = ex2(tmax);
     }
   } else if constexpr (C::kAnyQ4) {
     if (warp == 2 || warp == 3) {
@@ -831,7 +860,8 @@ __host__ __device__ __forceinline__ int build_segments(const PrefillArgs& a, int
   return ns;
 }
 // one tile of a piece, column-major so that a warp's 32 rows of one column are 128 contiguous
-// bytes: [D + 4 columns][128 rows] f32, columns O[0..D), frame, row sum, frame moves, pad
+// bytes: [D + 4 columns][128 rows] f32, columns O[0..D), frame, row sum, frame moves, log2 of
+// the largest P
 template <int D>
 __device__ __forceinline__ float* part_tile(float* part, int c, int slot, int t) {
   return part + ((static_cast<int64_t>(c) * 2 + slot) * 2 + t) * (D + 4) * kBM;
@@ -841,6 +871,30 @@ __device__ __forceinline__ float* part_tile(float* part, int c, int slot, int t)
 __device__ __forceinline__ void schedule_fault(volatile int* abort_flag) {
   *abort_flag = 1;
   atomicCAS(&g_prefill_error, kErrNone, kErrSchedule);
+}
+
+// Bounded wait (all lanes of the warp) for an appended block's flag, with acquire semantics;
+// then a proxy fence, so that the tensor copies this warp issues next read the stored block.
+// Gives up when the CTA aborts or after the wait limit (then records a timeout).
+__device__ __forceinline__ bool app_wait(const uint32_t* flag, volatile int* abort_flag) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  if (v == 0u) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      __nanosleep(64);
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+      if (v != 0u) break;
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicCAS(&g_prefill_error, kErrNone, kErrTimeout);
+        return false;
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
 }
 
 // Epilogue of one piece of a unit cut between CTAs, run by both tiles' softmax warps: store
@@ -853,9 +907,10 @@ __device__ __forceinline__ void schedule_fault(volatile int* abort_flag) {
 template <int D, bool BF16>
 __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
                                             uint32_t* pflags, uint32_t tag,
-                                            int32_t* rescale_count, void* o, int Hq, int Sq,
-                                            const SegS* sgp, uint32_t ocol, bool active, float f,
-                                            float l, int nres, uint32_t bar0, int pseg,
+                                            int32_t* rescale_count, float* p_max, void* o,
+                                            int Hq, int Sq, const SegS* sgp, uint32_t ocol,
+                                            bool active, float f, float l, int nres, float tmax,
+                                            uint32_t bar0, int pseg,
                                             volatile int* abort_flag,
                                             volatile uint32_t* merge_flag) {
   // everything else follows from the thread and the segment (kept out of the caller's registers)
@@ -888,6 +943,7 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
     pt[D * kBM] = active ? f : -INFINITY;
     pt[(D + 1) * kBM] = active ? l : 0.f;
     pt[(D + 2) * kBM] = __int_as_float(active ? nres : 0);
+    pt[(D + 3) * kBM] = active ? tmax : -INFINITY;
   }
   if (active) {
     // O has been read out of tensor memory: the next segment's PV may overwrite it
@@ -929,12 +985,14 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
     // frame moves: each piece counts its own first frame; the row as a whole counts one
     float L = 0.f;
     int moves = 1;
+    float T = -INFINITY;  // the largest P exponent of any piece (each relative to its own frame)
     for (int c = c_first; c <= c_last; ++c) {
       const float* pc = tile_of(c);
       const float fp = __ldcg(pc + D * kBM);
       if (fp == -INFINITY) continue;
       L = fmaf(ex2(fp - F), __ldcg(pc + (D + 1) * kBM), L);
       moves += __float_as_int(__ldcg(pc + (D + 2) * kBM)) - 1;
+      T = fmaxf(T, __ldcg(pc + (D + 3) * kBM));
     }
     const float inv_l = 1.f / L;
 #pragma unroll 1
@@ -963,6 +1021,7 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
       }
     }
     if (store && rescale_count) rescale_count[orow_idx] = moves;
+    if (store && p_max) p_max[orow_idx] = ex2(T);
   }
   if (merge && warp == 4) {
     // clear the unit's flags for the next call (or graph replay) with this tag
@@ -1047,6 +1106,48 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nseg = *seg_count;
+
+  if constexpr (KQ4 && VQ4) {
+    if (args.app_flags != nullptr) {
+      // ------------------------------------------------------------ phase 1: append the chunk
+      // items c, c + n_ctas, ...: every thread quantizes 32-element blocks of the item's rows
+      // (K, then V) with the cache builder's exact sequence; the item's flag is set once all
+      // of them are stored
+      constexpr int kNb = D / 32;
+      const int n_items = args.B * args.Hkv * args.app_nb;
+      for (int it = cta; it < n_items; it += args.n_ctas) {
+        const int bh = it / args.app_nb;  // b * Hkv + g
+        const int jb = args.app_j_lo + it % args.app_nb;
+        const int r0 = max(jb * kBN, args.app_pos0);
+        const int r1 = min((jb + 1) * kBN, args.app_pos0 + args.app_len);
+        const int per_side = (r1 - r0) * kNb;
+        for (int t = threadIdx.x; t < 2 * per_side; t += C::kThreads) {
+          const bool vside = t >= per_side;
+          const int tt = vside ? t - per_side : t;
+          const int row = r0 + tt / kNb;  // cache token
+          const int blk = tt % kNb;
+          const uint4* src = reinterpret_cast<const uint4*>(
+              (vside ? args.v_new : args.k_new) +
+              (static_cast<int64_t>(bh) * args.app_len + (row - args.app_pos0)) * D + blk * 32);
+          const uint4 w[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
+          uint4 nb;
+          __half sc;
+          q4_quantize_block<BF16>(w, nb, sc);
+          const int64_t crow = static_cast<int64_t>(bh) * args.Scap + row;
+          reinterpret_cast<uint4*>((vside ? args.v_nib : args.k_nib) + crow * (D / 2))[blk] = nb;
+          (vside ? args.v_scw : args.k_scw)[crow * kNb + blk] = sc;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          // the CTA's stores (observed through the barrier) before the flag, for the tensor
+          // copies and cp.async loads that other CTAs issue after reading it
+          __threadfence();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          st_release_gpu(args.app_flags + it, 1u);
+        }
+      }
+    }
+  }
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -1133,6 +1234,15 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       for (int j = sg.j0; j < sg.j1; ++j) {
+        if constexpr (KQ4 && VQ4) {
+          if (args.app_flags != nullptr && ok && j >= args.app_j_lo &&
+              j < args.app_j_lo + args.app_nb) {
+            // the block holds appended tokens: wait until phase 1 has stored them
+            ok = app_wait(args.app_flags + (b * args.Hkv + g) * args.app_nb + (j - args.app_j_lo),
+                          abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+          }
+        }
         produce(false, j);
         produce(true, j);
       }
@@ -1280,6 +1390,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       float f = -INFINITY;  // frame, base-2 units of the scaled score
       float l = 0.f;
       int nres = 0;
+      float tmax = -INFINITY;  // log2 of the largest P written
       for (int j = j0; j < e_t; ++j) {
         ok = mbar_wait(bar(kBarSFull + t), sf & 1, abort_flag, &g_prefill_error);
         ++sf;
@@ -1295,7 +1406,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
         // O holds this segment's earlier blocks when j > j0
         softmax_block<D, BF16, KQ4 != VQ4>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f, l,
-                                           nres);
+                                           nres, tmax);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarPReady + t));
@@ -1341,15 +1452,16 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
             }
           }
           if (store && args.rescale_count) args.rescale_count[orow_idx] = nres;
+          if (store && args.p_max) args.p_max[orow_idx] = ex2(tmax);
           // O has been read out of tensor memory: the next segment's PV may overwrite it
           tc_fence_before();
           mbar_arrive(bar(kBarOFree + t));
         }
       } else {
         ok = piece_epilogue<D, BF16>(args.W, args.n_ctas, args.part, args.pflags, args.tag,
-                                     args.rescale_count, args.o, args.Hq, args.Sq, segs + sidx,
-                                     ocol, active, f, l, nres, bar0, pseg, abort_flag,
-                                     merge_flag);
+                                     args.rescale_count, args.p_max, args.o, args.Hq, args.Sq,
+                                     segs + sidx, ocol, active, f, l, nres, tmax, bar0, pseg,
+                                     abort_flag, merge_flag);
         ++pseg;
       }
     }
@@ -1469,7 +1581,7 @@ static PrefillArgs schedule_args(int B, int Hq, int Hkv, int Sq, int Sk, int q_p
 }
 
 static Plan make_plan(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causal, int D,
-                      int num_sms) {
+                      int num_sms, bool force_cut = false) {
   const PrefillArgs a = schedule_args(B, Hq, Hq, Sq, Sk, q_pos_offset, causal);
   const int64_t per_class = static_cast<int64_t>(B) * Hq;
   Plan p;
@@ -1485,14 +1597,18 @@ static Plan make_plan(int B, int Hq, int Sq, int Sk, int q_pos_offset, int causa
   const int64_t per_cta = num_sms > 0 ? (p.W + num_sms - 1) / num_sms : 0;
   const bool fits = nb_min > 0 && (per_cta + nb_min - 1) / nb_min + 2 <= kMaxSegs;
   bool cuts = D == 128 && num_sms > 0 && p.units > num_sms && fits;
-  if (cuts) {
+  if (force_cut) {
+    cuts = D == 128 && num_sms > 0 && fits;
+  } else if (cuts) {
     const double avg = static_cast<double>(p.W) / static_cast<double>(p.units);
     const double whole_est = static_cast<double>((p.units + num_sms - 1) / num_sms) * avg;
     const double cut_est = static_cast<double>(per_cta) + 8.0 * (per_cta / avg + 1.0);
     cuts = cut_est < 0.97 * whole_est;
   }
   p.whole = !cuts;
-  p.n_ctas = p.whole ? 0 : num_sms;
+  // one CTA per SM, but never more CTAs than steps: every CTA's range must hold at least one
+  // step, since a unit's merge waits for every CTA between its first and its last piece
+  p.n_ctas = p.whole ? 0 : static_cast<int>(std::min<int64_t>(num_sms, p.W));
   p.flag_bytes = p.whole ? 0 : (static_cast<size_t>(p.n_ctas) * 2 * sizeof(uint32_t) + 255) /
                                    256 * 256;
   p.bytes = p.whole ? 0
@@ -1513,7 +1629,8 @@ int64_t prefill_debug_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int q_pos
   PrefillArgs a = schedule_args(B, Hq, Hkv, Sq, Sk, q_pos_offset, causal);
   const bool cut = !p.whole || (force_cut && num_sms > 0 && p.W > 0);
   a.W = p.W;
-  a.n_ctas = cut ? num_sms : 0;
+  // as in the launch: one CTA per SM, never more CTAs than steps
+  a.n_ctas = cut ? static_cast<int>(std::min<int64_t>(num_sms, p.W)) : 0;
   if (plan != nullptr) {
     plan[0] = p.whole ? 0 : 1;
     plan[1] = a.n_ctas;
@@ -1556,11 +1673,12 @@ static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  PrefillArgs a;
+  PrefillArgs a{};
   a.o = L.o;
   a.k_scale = static_cast<const uint8_t*>(L.k_scale);
   a.v_scale = static_cast<const uint8_t*>(L.v_scale);
   a.rescale_count = L.rescale_count;
+  a.p_max = L.p_max;
   a.B = L.B;
   a.Hq = L.Hq;
   a.Hkv = L.Hkv;
@@ -1599,11 +1717,12 @@ static cudaError_t launch_seg(const PrefillLaunch& L, const Plan& p, cudaStream_
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  PrefillArgs a;
+  PrefillArgs a{};
   a.o = L.o;
   a.k_scale = static_cast<const uint8_t*>(L.k_scale);
   a.v_scale = static_cast<const uint8_t*>(L.v_scale);
   a.rescale_count = L.rescale_count;
+  a.p_max = L.p_max;
   a.B = L.B;
   a.Hq = L.Hq;
   a.Hkv = L.Hkv;
@@ -1630,6 +1749,91 @@ static cudaError_t launch_seg_fmt(const PrefillLaunch& L, const Plan& p, cudaStr
                           : launch_seg<BF16, true, false>(L, p, stream);
   return L.vq4 ? launch_seg<BF16, false, true>(L, p, stream)
                : launch_seg<BF16, false, false>(L, p, stream);
+}
+
+// The append fused into the cut schedule: the cut is forced (every CTA takes part in phase 1)
+// and the launch is cooperative, so that all CTAs are resident together and a producer that
+// waits for another CTA's phase-1 item cannot wait on a CTA that has not started.
+static int app_blocks(int pos0, int len) { return (pos0 + len - 1) / kBN - pos0 / kBN + 1; }
+static size_t app_flag_bytes(int B, int Hkv, int pos0, int len) {
+  return (static_cast<size_t>(B) * Hkv * app_blocks(pos0, len) * sizeof(uint32_t) + 255) / 256 *
+         256;
+}
+
+size_t prefill_append_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int q_pos_offset,
+                                      int D, int num_sms) {
+  const Plan p = make_plan(B, Hq, Sq, Sk, q_pos_offset, 1, D, num_sms, true);
+  if (p.whole) return 0;
+  return p.bytes + app_flag_bytes(B, Hkv, q_pos_offset, Sq);
+}
+
+template <bool BF16>
+static cudaError_t launch_seg_append(const PrefillLaunch& L, const PrefillAppend& A,
+                                     const Plan& p, cudaStream_t stream) {
+  using C = Cfg<128, true, true>;
+  auto kern = prefill_seg_kernel<128, BF16, true, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  PrefillArgs a{};
+  a.o = L.o;
+  a.k_scale = static_cast<const uint8_t*>(L.k_scale);
+  a.v_scale = static_cast<const uint8_t*>(L.v_scale);
+  a.rescale_count = L.rescale_count;
+  a.p_max = L.p_max;
+  a.B = L.B;
+  a.Hq = L.Hq;
+  a.Hkv = L.Hkv;
+  a.Sq = L.Sq;
+  a.Sk = L.Sk;
+  a.Scap = L.Scap;
+  a.q_pos_offset = L.q_pos_offset;
+  a.causal = 1;
+  a.n_qtiles = (L.Sq + kBM - 1) / kBM;
+  a.n_pairs = (a.n_qtiles + 1) / 2;
+  a.scale_log2 = L.scale * kLog2e;
+  a.W = p.W;
+  a.n_ctas = p.n_ctas;
+  uint8_t* ws = static_cast<uint8_t*>(L.workspace);
+  a.pflags = reinterpret_cast<uint32_t*>(ws);
+  a.part = reinterpret_cast<float*>(ws + p.flag_bytes);
+  a.tag = L.tag;
+  a.k_new = static_cast<const uint16_t*>(A.k_new);
+  a.v_new = static_cast<const uint16_t*>(A.v_new);
+  a.k_nib = static_cast<uint8_t*>(A.k_nib);
+  a.v_nib = static_cast<uint8_t*>(A.v_nib);
+  a.k_scw = static_cast<__half*>(A.k_sc);
+  a.v_scw = static_cast<__half*>(A.v_sc);
+  a.app_flags = reinterpret_cast<uint32_t*>(ws + p.bytes);
+  a.app_pos0 = A.pos0;
+  a.app_len = A.len;
+  a.app_j_lo = A.pos0 / kBN;
+  a.app_nb = app_blocks(A.pos0, A.len);
+  e = cudaMemsetAsync(a.app_flags, 0, app_flag_bytes(L.B, L.Hkv, A.pos0, A.len), stream);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_ctas);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, L.tm_q, L.tm_k, L.tm_v, a);
+}
+
+cudaError_t prefill_append_launch(const PrefillLaunch& L, const PrefillAppend& A,
+                                  cudaStream_t stream) {
+  if (L.D != 128 || !L.kq4 || !L.vq4) return cudaErrorNotSupported;
+  const Plan p = make_plan(L.B, L.Hq, L.Sq, L.Sk, L.q_pos_offset, 1, L.D, L.num_sms, true);
+  if (p.whole) return cudaErrorNotSupported;
+  if (L.workspace == nullptr ||
+      L.workspace_bytes < p.bytes + app_flag_bytes(L.B, L.Hkv, A.pos0, A.len))
+    return cudaErrorInvalidValue;
+  return L.bf16 ? launch_seg_append<true>(L, A, p, stream)
+                : launch_seg_append<false>(L, A, p, stream);
 }
 
 cudaError_t prefill_launch(const PrefillLaunch& L, cudaStream_t stream) {

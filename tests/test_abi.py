@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     assert fa.fa_status_string(0) == "FA_OK"
     assert fa.fa_status_string(4) == "FA_ERR_TIMEOUT"
-    assert fa.fa_version() == 105
+    assert fa.fa_version() == 107
 
 
 def test_q4_0_sizes(lib):
@@ -162,3 +162,14 @@ def test_paged_decode_host_checks(lib):
     big_group[7], big_group[8] = 32, 2  # 16 query heads per kv head
     assert lib.fa_decode_paged(*big_group) == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_decode_paged_workspace_bytes(2, 8, 3, 128, 128, 8) == 0  # Hq % Hkv
+
+
+def test_library_needs_no_blas(lib):
+    """Every contraction of the library (the fused kernels and the explicit path's two GEMMs)
+    is its own tcgen05 code: the shared library neither links nor calls cuBLAS."""
+    needed = subprocess.run(["readelf", "-d", fa_build.LIB_PATH], capture_output=True, text=True,
+                            check=True).stdout
+    assert "cublas" not in needed.lower()
+    undefined = subprocess.run(["nm", "-D", "--undefined-only", fa_build.LIB_PATH],
+                               capture_output=True, text=True, check=True).stdout
+    assert "cublas" not in undefined.lower()

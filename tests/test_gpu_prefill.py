@@ -145,3 +145,42 @@ def test_prefill_repeated_calls_stay_exact(fa, shape):
     assert fa.fa_get_status() == fa.FA_OK
     for o in outs:
         check_close(np64(o), want, dtype, "repeated prefill")
+
+
+E10 = float(np.exp(10.0))
+
+
+@pytest.mark.parametrize("launch", ["whole_units", "cut_schedule"])
+@pytest.mark.parametrize("name", ["prefill_gqa32x8_d128_sq2048_sk16384_f16_ramp",
+                                  "prefill_gqa32x8_d128_sq2048_sk16384_f16"])
+def test_p_never_exceeds_e10(fa, name, launch):
+    """The deferred rescale keeps a row's frame until a block's maximum score outgrows it by the
+    10-point margin, so no P the softmax writes exceeds e^10 ("perf(rocm): defer SDPA
+    accumulator rescale, stage Q once per block (#2306)", What changed).  fa_fwd_kv_stats
+    reports every row's largest P: it must stay at or below e^10 (up to the rounding of the f32
+    exponent argument, < 2e-4 relative at these score magnitudes).  On the score ramp every row
+    carries its frame through blocks whose maximum climbs ~2 per block, so its largest P comes
+    close to the bound (above e^7 on every row); on N(0,1) data the first block sets the frame
+    and P stays far below it."""
+    w = fa_inputs.WORKLOADS[name]
+    q, k, v = fa_inputs.make_qkv(w, device="cuda", generate_on_device=True)
+    ws = None
+    if launch == "cut_schedule":
+        n = fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset, True)
+        assert n > 0
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    pm = torch.full((w.B, w.Hq, w.Sq), -1.0, dtype=torch.float32, device="cuda")
+    rc = torch.full((w.B, w.Hq, w.Sq), -1, dtype=torch.int32, device="cuda")
+    o = fa.fa_fwd_kv(q, k, v, causal=True, q_pos_offset=w.q_pos_offset, workspace=ws,
+                     rescale_count=rc, p_max=pm)
+    plain = fa.fa_fwd_kv(q, k, v, causal=True, q_pos_offset=w.q_pos_offset, workspace=ws)
+    assert fa.fa_get_status() == fa.FA_OK
+    assert torch.equal(o, plain), "reporting the statistic changed the result"
+    p = pm.cpu().numpy()
+    assert np.isfinite(p).all() and p.min() >= 1.0 - 1e-6, p.min()
+    assert p.max() <= E10 * (1 + 2e-4), p.max()
+    if w.ramp:
+        assert p.min() > np.exp(7.0), p.min()
+        assert (rc.cpu().numpy() >= 2).all()
+    else:
+        assert p.max() < np.exp(8.0), p.max()

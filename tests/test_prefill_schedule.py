@@ -187,3 +187,16 @@ def test_invalid_arguments(args):
     with pytest.raises(fa.FaError) as e:
         fa.fa_prefill_schedule(*args)
     assert e.value.status == fa.FA_ERR_INVALID_ARG
+
+
+def test_cut_never_has_more_ctas_than_steps():
+    """A cut over more CTAs than key-block steps would leave CTAs with empty ranges between a
+    unit's pieces, whose merge waits for every CTA in between: the schedule then uses one CTA
+    per step (the fused append forces the cut on small chunks)."""
+    B, Hq, Hkv, Sq, Sk, D, off = 2, 8, 4, 300, 429, 128, 129
+    W, _ = expected_segments(units_of(B, Hq, Sq, Sk, off, True), 1)
+    assert W < 152
+    plan, rows = fa.fa_prefill_schedule(B, Hq, Hkv, Sq, Sk, D, off, True, 152, force_cut=True)
+    assert plan["ctas"] == W
+    assert sorted(set(int(c) for c in rows[:, 0])) == list(range(W))
+    check_schedule(B, Hq, Hkv, Sq, Sk, D, off, True, W, force=True)
