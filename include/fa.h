@@ -122,16 +122,21 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, int B,
                     void* workspace, size_t workspace_bytes, int32_t* rescale_count,
                     fa_stream_t stream);
 
-/* fa_fwd_kv that also reports, per query row, the largest softmax numerator P it produced.
- * The deferred rescale of "perf(rocm): defer SDPA accumulator rescale, stage Q once per block
- * (#2306)" (What changed) keeps a row's frame f until a key block's maximum score exceeds it by
- * more than 10 natural-log units, so every P = e^(s - f) the kernel writes stays at or below
- * e^10 = 22026.47 (up to the rounding of the f32 exponent argument).  This call exposes that
- * bound for testing.
- *  p_max : optional device float [B, Hq, Sq] (NULL to skip): for every query row the largest P
- *          value (before its rounding to the dtype) over all its key blocks, each relative to the
- *          frame in force for that block; where the cut schedule splits a row between CTAs, the
- *          largest over the pieces.  Not written when Sq == 1.
+/* fa_fwd_kv that also reports, per query row, a bound on the largest softmax numerator P it
+ * produced.  The deferred rescale of "perf(rocm): defer SDPA accumulator rescale, stage Q once
+ * per block (#2306)" (What changed) keeps a row's frame f until a key block's maximum score
+ * exceeds it by more than 10 natural-log units, so every P = e^(s - f) the kernel writes stays
+ * at or below e^10 = 22026.47 (up to the rounding of the f32 exponent argument).  This call
+ * exposes that bound for testing.
+ *  p_max : optional device float [B, Hq, Sq] (NULL to skip): for every query row the largest,
+ *          over its key blocks, of a per-block value that is at least the block's largest P
+ *          (before its rounding to the dtype, in the frame in force for that block): the
+ *          block's largest P where the kernel tested the block's max against the frame, its
+ *          sum of P where the sum already showed that no P can reach the bound (the kernels
+ *          form P in the current frame first and run the frame test only when a block's sum
+ *          exceeds 21 800, just below e^10).  Where the cut schedule splits a row between CTAs,
+ *          the largest over the pieces.  So p_max <= e^10 holds exactly when no written P
+ *          exceeds e^10 by more than the rounding above.  Not written when Sq == 1.
  *  Other arguments, scratch, errors: as fa_fwd_kv (which is this call with p_max = NULL). */
 fa_status fa_fwd_kv_stats(const void* q, const void* k, const void* v, void* o, int B, int Hq,
                           int Hkv, int Sq, int Sk, int kv_capacity, int D, int q_pos_offset,

@@ -104,6 +104,58 @@ __global__ void __launch_bounds__(256) softmax_kernel(const float* __restrict__ 
   for (int j = tid; j < Skp; j += 256) p[j] = to_bits<BF16>(j < lim ? __expf(s[j] - m) * inv : 0.f);
 }
 
+// The same row softmax with the row held in registers: one read of S and one write of P per
+// element (the kernel above reads S three times).  kVpt values per thread, thread j holding
+// columns j, j + threads, ...; used when Skp <= kVpt * 1024.
+constexpr int kVpt = 32;
+template <bool BF16>
+__global__ void __launch_bounds__(1024) softmax_regs_kernel(const float* __restrict__ S,
+                                                            uint16_t* __restrict__ P, int Sq,
+                                                            int Sk, int Skp, int q_pos_offset,
+                                                            int causal) {
+  const int64_t row = blockIdx.x;
+  const int i = static_cast<int>(row % Sq);
+  const int lim = causal ? min(Sk, q_pos_offset + i + 1) : Sk;  // visible keys [0, lim)
+  const float* s = S + row * Skp;
+  uint16_t* p = P + row * Skp;
+  __shared__ float red[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+  const int nwarps = nt >> 5;
+  float v[kVpt];
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kVpt; ++k) {
+    const int j = tid + k * nt;
+    v[k] = (j < lim) ? __ldcs(s + j) : -INFINITY;  // S is read once: streaming loads
+    m = fmaxf(m, v[k]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = red[0];
+  for (int w = 1; w < nwarps; ++w) m = fmaxf(m, red[w]);
+  __syncthreads();
+  float l = 0.f;
+#pragma unroll
+  for (int k = 0; k < kVpt; ++k) {
+    v[k] = __expf(v[k] - m);  // 0 at masked keys
+    l += v[k];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  if (lane == 0) red[warp] = l;
+  __syncthreads();
+  l = 0.f;
+  for (int w = 0; w < nwarps; ++w) l += red[w];
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int k = 0; k < kVpt; ++k) {
+    const int j = tid + k * nt;
+    if (j < Skp) p[j] = to_bits<BF16>(v[k] * inv);
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // tcgen05 GEMM
 // ------------------------------------------------------------------------------------------
@@ -145,6 +197,7 @@ __device__ __forceinline__ int tile_i_max(const GemmArgs& a, int m0) {
 template <int BN, bool BF16, bool B_MN, bool OUT_F32>
 __global__ void __launch_bounds__(kGThreads) gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                                                          const __grid_constant__ CUtensorMap tm_b,
+                                                         const __grid_constant__ CUtensorMap tm_c,
                                                          const GemmArgs args) {
   using C = GCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -257,7 +310,7 @@ __global__ void __launch_bounds__(kGThreads) gemm_kernel(const __grid_constant__
 
   // ---------------------------------------------------------------- epilogue, all four warps
   ok = !*abort_flag && mbar_wait(acc_full, 0, abort_flag, &g_explicit_error);
-  ok = __all_sync(0xffffffffu, ok);
+  ok = __syncthreads_and(ok) != 0;  // the epilogue's barriers need every thread, or none
   if (ok) {
     tc_fence_after();
     const int row = m0 + 32 * warp + lane;
@@ -269,17 +322,43 @@ __global__ void __launch_bounds__(kGThreads) gemm_kernel(const __grid_constant__
       tmem_ld32(taddr + c0, r);
       tmem_wait_ld();
       reg_fence32(r);
-      if (!store || n0 + c0 >= args.N) continue;
       if (OUT_F32) {
-        float* dst = static_cast<float*>(args.c) + grp * args.c_group + row * args.ldc + n0 + c0;
+        // f32 tile: 32 columns of the 128 rows go to shared memory (128-byte swizzle: a row's
+        // 16-byte chunk c sits at chunk c ^ (row % 8), conflict-free for one row per thread)
+        // and leave by one tensor store, two buffers alternating; the ring is idle by now
+        const int buf = (c0 / 32) & 1;
+        const uint32_t sbuf = sbase + buf * (kGM * 128);
+        if (c0 >= 64) {
+          // the store issued from this buffer two chunks ago has read it
+          if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          asm volatile("bar.sync 1, %0;" ::"n"(kGThreads) : "memory");
+        }
+        const int rl = 32 * warp + lane;  // row within the tile
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          reinterpret_cast<float4*>(dst)[i] =
-              make_float4(__uint_as_float(r[4 * i]) * args.alpha,
-                          __uint_as_float(r[4 * i + 1]) * args.alpha,
-                          __uint_as_float(r[4 * i + 2]) * args.alpha,
-                          __uint_as_float(r[4 * i + 3]) * args.alpha);
-      } else {
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t a = sbuf + rl * 128 + ((i ^ (rl & 7)) << 4);
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                       "f"(__uint_as_float(r[4 * i]) * args.alpha),
+                       "f"(__uint_as_float(r[4 * i + 1]) * args.alpha),
+                       "f"(__uint_as_float(r[4 * i + 2]) * args.alpha),
+                       "f"(__uint_as_float(r[4 * i + 3]) * args.alpha)
+                       : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kGThreads) : "memory");
+        if (threadIdx.x == 0 && n0 + c0 < args.N) {
+          // rows past M and columns past N are clipped by the tensor store
+          asm volatile(
+              "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+              ::"l"(reinterpret_cast<uint64_t>(&tm_c)), "r"(n0 + c0), "r"(m0), "r"(grp),
+              "r"(sbuf)
+              : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        continue;
+      }
+      if (!store || n0 + c0 >= args.N) continue;
+      {
         uint16_t* dst =
             static_cast<uint16_t*>(args.c) + grp * args.c_group + row * args.ldc + n0 + c0;
         uint32_t pk[16];
@@ -294,6 +373,8 @@ __global__ void __launch_bounds__(kGThreads) gemm_kernel(const __grid_constant__
       }
     }
   }
+  if (OUT_F32 && threadIdx.x == 0)
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the tile's stores are done
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -303,15 +384,15 @@ __global__ void __launch_bounds__(kGThreads) gemm_kernel(const __grid_constant__
 }
 
 template <int BN, bool BF16, bool B_MN, bool OUT_F32>
-cudaError_t gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                        int groups, cudaStream_t stream) {
+cudaError_t gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                        const GemmArgs& a, int groups, cudaStream_t stream) {
   using C = GCfg<BN>;
   auto kern = gemm_kernel<BN, BF16, B_MN, OUT_F32>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.N + BN - 1) / BN, (a.M + kGM - 1) / kGM, groups);
-  kern<<<grid, kGThreads, C::kSmemBytes, stream>>>(ta, tb, a);
+  kern<<<grid, kGThreads, C::kSmemBytes, stream>>>(ta, tb, tc, a);
   return cudaGetLastError();
 }
 
@@ -375,8 +456,9 @@ cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* m
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   // S = scale Q_g K^T: A = Q_g [M][D], B = K [Sk][D] (K-major), C = S [M][Skp] f32; tiles of
   // 128 keys, the last one covering the padding
-  CUtensorMap tq, tk, tp, tv;
-  if (!encode_map_3d(&tq, L.q, tdt, 2, L.D, M, groups, kGK, kGM, sw) ||
+  CUtensorMap tq, tk, tp, tv, ts;
+  if (!encode_map_3d(&ts, S, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Skp, M, groups, 32, kGM, sw) ||
+      !encode_map_3d(&tq, L.q, tdt, 2, L.D, M, groups, kGK, kGM, sw) ||
       !encode_map_3d(&tk, K, tdt, 2, L.D, L.Sk, groups, kGK, 128, sw) ||
       !encode_map_3d(&tp, P, tdt, 2, Skp, M, groups, kGK, kGM, sw) ||
       !encode_map_3d(&tv, V, tdt, 2, L.D, L.Sk, groups, 64, kGK, sw)) {
@@ -395,15 +477,25 @@ cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* m
   ga.q_pos_offset = L.q_pos_offset;
   ga.causal = L.causal;
   ga.k_is_keys = 0;
-  e = L.bf16 ? gemm_launch<128, true, false, true>(tq, tk, ga, groups, stream)
-             : gemm_launch<128, false, false, true>(tq, tk, ga, groups, stream);
+  e = L.bf16 ? gemm_launch<128, true, false, true>(tq, tk, ts, ga, groups, stream)
+             : gemm_launch<128, false, false, true>(tq, tk, ts, ga, groups, stream);
   if (e != cudaSuccess) return e;
-  if (L.bf16)
+  if (Skp <= kVpt * 1024) {
+    // one warp per 32 x kVpt columns (Skp is a multiple of 64)
+    const int nt = (Skp + kVpt * 32 - 1) / (kVpt * 32) * 32;
+    if (L.bf16)
+      softmax_regs_kernel<true><<<static_cast<unsigned>(rows), nt, 0, stream>>>(
+          S, P, L.Sq, L.Sk, Skp, L.q_pos_offset, L.causal);
+    else
+      softmax_regs_kernel<false><<<static_cast<unsigned>(rows), nt, 0, stream>>>(
+          S, P, L.Sq, L.Sk, Skp, L.q_pos_offset, L.causal);
+  } else if (L.bf16) {
     softmax_kernel<true><<<static_cast<unsigned>(rows), 256, 0, stream>>>(
         S, P, L.Sq, L.Sk, Skp, L.q_pos_offset, L.causal);
-  else
+  } else {
     softmax_kernel<false><<<static_cast<unsigned>(rows), 256, 0, stream>>>(
         S, P, L.Sq, L.Sk, Skp, L.q_pos_offset, L.causal);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // O_g = P_g V: A = P_g [M][Skp], B = V [Sk][D] (MN-major; keys past Sk read as zeros, where
@@ -416,11 +508,12 @@ cudaError_t explicit_launch(const ExplicitLaunch& L, cudaStream_t stream, int* m
   go.K = Skp;
   go.alpha = 1.f;
   go.k_is_keys = 1;
+  // (the O GEMM writes with plain stores: its tensor-store map is unused)
   if (L.D == 128)
-    return L.bf16 ? gemm_launch<128, true, true, false>(tp, tv, go, groups, stream)
-                  : gemm_launch<128, false, true, false>(tp, tv, go, groups, stream);
-  return L.bf16 ? gemm_launch<64, true, true, false>(tp, tv, go, groups, stream)
-                : gemm_launch<64, false, true, false>(tp, tv, go, groups, stream);
+    return L.bf16 ? gemm_launch<128, true, true, false>(tp, tv, ts, go, groups, stream)
+                  : gemm_launch<128, false, true, false>(tp, tv, ts, go, groups, stream);
+  return L.bf16 ? gemm_launch<64, true, true, false>(tp, tv, ts, go, groups, stream)
+                : gemm_launch<64, false, true, false>(tp, tv, ts, go, groups, stream);
 }
 
 uint32_t explicit_take_error() {

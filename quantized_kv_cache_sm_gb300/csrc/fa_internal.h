@@ -19,7 +19,7 @@ struct PrefillLaunch {
   const void* k_scale;           // scale plane of a q4_0 K (else null)
   const void* v_scale;           // scale plane of a q4_0 V (else null)
   int32_t* rescale_count;
-  float* p_max;                  // optional per-row largest P (see fa_fwd_kv_stats)
+  float* p_max;                  // optional per-row bound on the largest P (fa_fwd_kv_stats)
   int B, Hq, Hkv, Sq, Sk, Scap, D, q_pos_offset, causal;  // Scap: K/V tokens per (b, kv head)
   float scale;
   bool bf16, kq4, vq4;

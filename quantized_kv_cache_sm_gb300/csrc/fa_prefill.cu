@@ -105,7 +105,8 @@ struct PrefillArgs {
   const uint8_t* k_scale;  // q4_0 only: fp16 scale planes [B, Hkv, Sk, D/32]
   const uint8_t* v_scale;
   int32_t* rescale_count;  // optional [B, Hq, Sq]
-  float* p_max;            // optional [B, Hq, Sq]: the largest P the row's softmax produced
+  float* p_max;            // optional [B, Hq, Sq]: a bound on the largest P the row's softmax
+                           // wrote (see softmax_block)
   int B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, n_qtiles, n_pairs;
   int Scap;  // tokens per (batch, kv head) in the K/V tensors (row stride); Sk <= Scap
   float scale_log2;
@@ -244,45 +245,6 @@ __device__ __forceinline__ float block_row_exp(uint32_t scol, int rel_lim, float
   return a.x + a.y;
 }
 
-// Single-read form of the two passes above: the row's 128 scores of S(j) read from TMEM with
-// one wait (keys past rel_lim set to -inf when MASK) and kept in registers for the
-// exponentials.  Same values, same summation order.
-template <bool MASK>
-__device__ __forceinline__ float block_row_load(uint32_t scol, int rel_lim, float (&s)[kBN]) {
-  uint32_t r0[32], r1[32], r2[32], r3[32];
-  tmem_ld32(scol, r0);
-  tmem_ld32(scol + 32, r1);
-  tmem_ld32(scol + 64, r2);
-  tmem_ld32(scol + 96, r3);
-  tmem_wait_ld();
-  reg_fence32(r0);
-  reg_fence32(r1);
-  reg_fence32(r2);
-  reg_fence32(r3);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    s[i] = __uint_as_float(r0[i]);
-    s[32 + i] = __uint_as_float(r1[i]);
-    s[64 + i] = __uint_as_float(r2[i]);
-    s[96 + i] = __uint_as_float(r3[i]);
-    if (MASK) {
-      if (i > rel_lim) s[i] = -INFINITY;
-      if (32 + i > rel_lim) s[32 + i] = -INFINITY;
-      if (64 + i > rel_lim) s[64 + i] = -INFINITY;
-      if (96 + i > rel_lim) s[96 + i] = -INFINITY;
-    }
-  }
-  // four independent chains, two new scores per three-input max
-  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    m0 = fmax3(m0, s[i], s[i + 1]);
-    m1 = fmax3(m1, s[32 + i], s[33 + i]);
-    m2 = fmax3(m2, s[64 + i], s[65 + i]);
-    m3 = fmax3(m3, s[96 + i], s[97 + i]);
-  }
-  return fmax3(fmaxf(m0, m1), m2, m3);
-}
 template <bool BF16>
 __device__ __forceinline__ float block_row_exp_regs(uint32_t scol, const float (&s)[kBN],
                                                     float sl2, float nf) {
@@ -307,27 +269,75 @@ __device__ __forceinline__ float block_row_exp_regs(uint32_t scol, const float (
   return a.x + a.y;
 }
 
+// the scores of S(j) for this row with one TMEM wait, keys past rel_lim set to -inf (MASK)
+template <bool MASK>
+__device__ __forceinline__ void block_row_scores(uint32_t scol, int rel_lim, float (&s)[kBN]) {
+  uint32_t r0[32], r1[32], r2[32], r3[32];
+  tmem_ld32(scol, r0);
+  tmem_ld32(scol + 32, r1);
+  tmem_ld32(scol + 64, r2);
+  tmem_ld32(scol + 96, r3);
+  tmem_wait_ld();
+  reg_fence32(r0);
+  reg_fence32(r1);
+  reg_fence32(r2);
+  reg_fence32(r3);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    s[i] = __uint_as_float(r0[i]);
+    s[32 + i] = __uint_as_float(r1[i]);
+    s[64 + i] = __uint_as_float(r2[i]);
+    s[96 + i] = __uint_as_float(r3[i]);
+    if (MASK) {
+      if (i > rel_lim) s[i] = -INFINITY;
+      if (32 + i > rel_lim) s[32 + i] = -INFINITY;
+      if (64 + i > rel_lim) s[64 + i] = -INFINITY;
+      if (96 + i > rel_lim) s[96 + i] = -INFINITY;
+    }
+  }
+}
+__device__ __forceinline__ float row_max_regs(const float (&s)[kBN]) {
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    m0 = fmax3(m0, s[i], s[i + 1]);
+    m1 = fmax3(m1, s[32 + i], s[33 + i]);
+    m2 = fmax3(m2, s[64 + i], s[65 + i]);
+    m3 = fmax3(m3, s[96 + i], s[97 + i]);
+  }
+  return fmax3(fmaxf(m0, m1), m2, m3);
+}
+
+// Single-read form: a block's P is first formed in the row's current frame f.  Its row sum can exceed
+// kSumTrigger only when some P does, and every P stays below 2^margin = e^10 unless the block
+// max outgrows the frame by more than the margin; so a warp in which no row's sum exceeds it
+// keeps those P without ever forming the block max.  Otherwise (or on a row's first block,
+// f = -inf) the frame test proper runs: the block max, the frame move when it exceeds f by
+// more than the margin, and P formed again in the new frame.  The frame decisions are exactly
+// those of testing every block's max.  kSumTrigger sits just below e^10, so that the rounding
+// of the exponential cannot hide a P at the bound.
+constexpr float kSumTrigger = 21800.f;
+
 // One key block of the online softmax for this thread's query row: read S(j), move the frame f
 // to the block max when that exceeds f by more than the margin (l and, when it already holds
 // earlier blocks (o_live), O are scaled by 2^(f_old - f)), write P = 2^(s - f) over S and add
 // its row sum to l.  O may be rescaled in place: S(j) being ready means PV(j-1) has completed
 // (QK(j) was issued after it).  The caller waits for the TMEM stores.
 //
-// ONE_READ selects the single-read form (one TMEM wait per block, 128 scores in registers)
-// over the two-pass form (six waits, fewer live registers).  Measured per kernel: the single
-// read is faster in the one-unit-per-CTA kernel and in the cut-schedule kernel with exactly
-// one q4_0 side (by 11 % with a q4_0 V), slower by 2 % in the dense cut-schedule kernel, even
-// with q4_0 on both sides.
+// ONE_READ selects the single-read form (one TMEM wait per block, 128 scores in registers,
+// P formed in the current frame first) over the two-pass form (the row max from tensor memory,
+// then P: six waits, fewer live registers).  Measured per kernel: the single read is faster in
+// the one-unit-per-CTA kernel and in the cut-schedule kernel with at least one dense side, the
+// two passes in the cut-schedule kernel with q4_0 K and V.
 //
-// tmax tracks the base-2 exponent of the largest P written so far, t = s_max * sl2 - f taken
-// after the frame test (P is monotonic in the score, so the block's largest P is that of its
-// largest score; t is formed from the rounded s_max * sl2 the frame test uses, so it can differ
-// from the exponent of the stored P by an f32 rounding); the frame rule keeps t <= the margin,
-// so P <= e^10.
+// pmx tracks a bound on the largest P written (before its rounding to the dtype), each in the
+// frame in force for its block: the exact largest P of a block that ran the frame test (P is
+// monotonic in the score), the block's sum of P otherwise (at least its largest P, and below
+// kSumTrigger).  Either way pmx <= e^10 whenever the frame rule holds.
 template <int D, bool BF16, bool ONE_READ>
 __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool need_mask,
                                               int rel_lim, float sl2, bool o_live, float& f,
-                                              float& l, int& nres, float& tmax) {
+                                              float& l, int& nres, float& pmx) {
   auto rescale_o = [&](float alpha) {
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
@@ -340,47 +350,57 @@ __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool
       tmem_st32(ocol + 32 * c, r);
     }
   };
-  if constexpr (ONE_READ) {
-    float s[kBN];
-    float mx;
-    if (need_mask)
-      mx = block_row_load<true>(scol, rel_lim, s);
-    else
-      mx = block_row_load<false>(scol, rel_lim, s);
+  // the frame test proper: block max mx (scaled to m2), frame move, O rescale; true if any row
+  // of the warp moved its frame
+  auto frame_test = [&](float mx, float& alpha) -> bool {
     const float m2 = mx * sl2;
     const bool need = m2 > f + kMarginLog2;
-    const bool any = __any_sync(0xffffffffu, need);
-    float alpha = 1.f;
+    alpha = 1.f;
     if (need) {
       alpha = ex2(f - m2);
       l *= alpha;
       f = m2;
       ++nres;
     }
-    tmax = fmaxf(tmax, m2 - f);  // -inf for a fully masked row block; NaN (ignored) if also f
-    l += block_row_exp_regs<BF16>(scol, s, sl2, -f);
-    if (any && o_live) rescale_o(alpha);
+    return __any_sync(0xffffffffu, need);
+  };
+  if constexpr (ONE_READ) {
+    const bool first = __any_sync(0xffffffffu, f == -INFINITY);
+    float s[kBN];
+    if (need_mask)
+      block_row_scores<true>(scol, rel_lim, s);
+    else
+      block_row_scores<false>(scol, rel_lim, s);
+    float sum = 0.f;
+    bool done = false;
+    if (!first) {
+      sum = block_row_exp_regs<BF16>(scol, s, sl2, -f);
+      done = !__any_sync(0xffffffffu, sum > kSumTrigger);
+    }
+    if (done) {
+      pmx = fmaxf(pmx, sum);
+    } else {
+      const float mx = row_max_regs(s);
+      float alpha;
+      const bool any = frame_test(mx, alpha);
+      if (any || first) {
+        sum = block_row_exp_regs<BF16>(scol, s, sl2, -f);
+        if (any && o_live) rescale_o(alpha);
+      }
+      pmx = fmaxf(pmx, ex2(fmaf(mx, sl2, -f)));  // -inf keys (a masked row) give 0
+    }
+    l += sum;
   } else {
-    // pass 1: row max over the 128 scores
+    // two passes over S in tensor memory: the row max (and the frame test) first, then P
     const float mx = need_mask ? block_row_max<true>(scol, rel_lim)
                                : block_row_max<false>(scol, rel_lim);
-    const float m2 = mx * sl2;
-    const bool need = m2 > f + kMarginLog2;
-    if (__any_sync(0xffffffffu, need)) {
-      const float alpha = need ? ex2(f - m2) : 1.f;
-      if (need) {
-        l *= alpha;
-        f = m2;
-        ++nres;
-      }
-      if (o_live) {
-        rescale_o(alpha);
-        tmem_wait_st();
-      }
+    float alpha;
+    if (frame_test(mx, alpha) && o_live) {
+      rescale_o(alpha);
+      tmem_wait_st();
     }
-    tmax = fmaxf(tmax, m2 - f);  // -inf for a fully masked row block; NaN (ignored) if also f
-    // pass 2: P = 2^(t - f) over the first half of S, row sum
     const float nf = -f;
+    pmx = fmaxf(pmx, ex2(fmaf(mx, sl2, nf)));
     l += need_mask ? block_row_exp<true, BF16>(scol, rel_lim, sl2, nf)
                    : block_row_exp<false, BF16>(scol, rel_lim, sl2, nf);
   }
@@ -635,7 +655,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
     float f = -INFINITY;  // frame, base-2 units of the scaled score
     float l = 0.f;
     int nres = 0;
-    float tmax = -INFINITY;  // log2 of the largest P written
+    float pmx = -INFINITY;  // bound on the largest P written
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       ok = mbar_wait(bar(kBarSFull + t), j & 1, abort_flag, &g_prefill_error);
@@ -650,7 +670,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       // last visible key of this row, relative to the block
       const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
       softmax_block<D, BF16, true>(scol, ocol, need_mask, rel_lim, sl2, j > 0, f, l, nres,
-                                   tmax);
+                                   pmx);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPReady + t));
@@ -687,7 +707,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       if (store && args.rescale_count)
         args.rescale_count[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = nres;
       if (store && args.p_max)
-        args.p_max[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = ex2(tmax);
+        args.p_max[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = pmx;
     }
   } else if constexpr (C::kAnyQ4) {
     if (warp == 2 || warp == 3) {
@@ -860,8 +880,8 @@ __host__ __device__ __forceinline__ int build_segments(const PrefillArgs& a, int
   return ns;
 }
 // one tile of a piece, column-major so that a warp's 32 rows of one column are 128 contiguous
-// bytes: [D + 4 columns][128 rows] f32, columns O[0..D), frame, row sum, frame moves, log2 of
-// the largest P
+// bytes: [D + 4 columns][128 rows] f32, columns O[0..D), frame, row sum, frame moves, the
+// bound on the largest P
 template <int D>
 __device__ __forceinline__ float* part_tile(float* part, int c, int slot, int t) {
   return part + ((static_cast<int64_t>(c) * 2 + slot) * 2 + t) * (D + 4) * kBM;
@@ -909,7 +929,7 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
                                             uint32_t* pflags, uint32_t tag,
                                             int32_t* rescale_count, float* p_max, void* o,
                                             int Hq, int Sq, const SegS* sgp, uint32_t ocol,
-                                            bool active, float f, float l, int nres, float tmax,
+                                            bool active, float f, float l, int nres, float pmx,
                                             uint32_t bar0, int pseg,
                                             volatile int* abort_flag,
                                             volatile uint32_t* merge_flag) {
@@ -943,7 +963,7 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
     pt[D * kBM] = active ? f : -INFINITY;
     pt[(D + 1) * kBM] = active ? l : 0.f;
     pt[(D + 2) * kBM] = __int_as_float(active ? nres : 0);
-    pt[(D + 3) * kBM] = active ? tmax : -INFINITY;
+    pt[(D + 3) * kBM] = active ? pmx : -INFINITY;
   }
   if (active) {
     // O has been read out of tensor memory: the next segment's PV may overwrite it
@@ -985,7 +1005,7 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
     // frame moves: each piece counts its own first frame; the row as a whole counts one
     float L = 0.f;
     int moves = 1;
-    float T = -INFINITY;  // the largest P exponent of any piece (each relative to its own frame)
+    float T = -INFINITY;  // the pieces' bounds on their largest P (each in its own frame)
     for (int c = c_first; c <= c_last; ++c) {
       const float* pc = tile_of(c);
       const float fp = __ldcg(pc + D * kBM);
@@ -1021,7 +1041,7 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
       }
     }
     if (store && rescale_count) rescale_count[orow_idx] = moves;
-    if (store && p_max) p_max[orow_idx] = ex2(T);
+    if (store && p_max) p_max[orow_idx] = T;
   }
   if (merge && warp == 4) {
     // clear the unit's flags for the next call (or graph replay) with this tag
@@ -1106,48 +1126,6 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nseg = *seg_count;
-
-  if constexpr (KQ4 && VQ4) {
-    if (args.app_flags != nullptr) {
-      // ------------------------------------------------------------ phase 1: append the chunk
-      // items c, c + n_ctas, ...: every thread quantizes 32-element blocks of the item's rows
-      // (K, then V) with the cache builder's exact sequence; the item's flag is set once all
-      // of them are stored
-      constexpr int kNb = D / 32;
-      const int n_items = args.B * args.Hkv * args.app_nb;
-      for (int it = cta; it < n_items; it += args.n_ctas) {
-        const int bh = it / args.app_nb;  // b * Hkv + g
-        const int jb = args.app_j_lo + it % args.app_nb;
-        const int r0 = max(jb * kBN, args.app_pos0);
-        const int r1 = min((jb + 1) * kBN, args.app_pos0 + args.app_len);
-        const int per_side = (r1 - r0) * kNb;
-        for (int t = threadIdx.x; t < 2 * per_side; t += C::kThreads) {
-          const bool vside = t >= per_side;
-          const int tt = vside ? t - per_side : t;
-          const int row = r0 + tt / kNb;  // cache token
-          const int blk = tt % kNb;
-          const uint4* src = reinterpret_cast<const uint4*>(
-              (vside ? args.v_new : args.k_new) +
-              (static_cast<int64_t>(bh) * args.app_len + (row - args.app_pos0)) * D + blk * 32);
-          const uint4 w[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
-          uint4 nb;
-          __half sc;
-          q4_quantize_block<BF16>(w, nb, sc);
-          const int64_t crow = static_cast<int64_t>(bh) * args.Scap + row;
-          reinterpret_cast<uint4*>((vside ? args.v_nib : args.k_nib) + crow * (D / 2))[blk] = nb;
-          (vside ? args.v_scw : args.k_scw)[crow * kNb + blk] = sc;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          // the CTA's stores (observed through the barrier) before the flag, for the tensor
-          // copies and cp.async loads that other CTAs issue after reading it
-          __threadfence();
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          st_release_gpu(args.app_flags + it, 1u);
-        }
-      }
-    }
-  }
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -1369,6 +1347,51 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
     }
   } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------------- softmax rows
+    if constexpr (KQ4 && VQ4) {
+      if (args.app_flags != nullptr) {
+        // -------------------------------------------------------- phase 1: append the chunk
+        // done by the 256 softmax threads while the producer and the MMA issuer fill the
+        // pipeline: items c, c + n_ctas, ...: every thread quantizes 32-element blocks of the
+        // item's rows (K, then V) with the cache builder's exact sequence; the item's flag is
+        // set once all of them are stored
+        constexpr int kNb = D / 32;
+        const int st = threadIdx.x - 4 * 32;  // 0..255
+        const int n_items = args.B * args.Hkv * args.app_nb;
+        for (int it = cta; it < n_items; it += args.n_ctas) {
+          const int bh = it / args.app_nb;  // b * Hkv + g
+          const int jb = args.app_j_lo + it % args.app_nb;
+          const int r0 = max(jb * kBN, args.app_pos0);
+          const int r1 = min((jb + 1) * kBN, args.app_pos0 + args.app_len);
+          const int per_side = (r1 - r0) * kNb;
+          for (int t = st; t < 2 * per_side; t += 256) {
+            const bool vside = t >= per_side;
+            const int tt = vside ? t - per_side : t;
+            const int row = r0 + tt / kNb;  // cache token
+            const int blk = tt % kNb;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                (vside ? args.v_new : args.k_new) +
+                (static_cast<int64_t>(bh) * args.app_len + (row - args.app_pos0)) * D +
+                blk * 32);
+            const uint4 w[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
+            uint4 nb;
+            __half sc;
+            q4_quantize_block<BF16>(w, nb, sc);
+            const int64_t crow = static_cast<int64_t>(bh) * args.Scap + row;
+            reinterpret_cast<uint4*>((vside ? args.v_nib : args.k_nib) + crow * (D / 2))[blk] =
+                nb;
+            (vside ? args.v_scw : args.k_scw)[crow * kNb + blk] = sc;
+          }
+          asm volatile("bar.sync 2, 256;" ::: "memory");  // the 256 softmax threads
+          if (st == 0) {
+            // their stores (observed through the barrier) before the flag, for the tensor
+            // copies and cp.async loads that other CTAs issue after reading it
+            __threadfence();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            st_release_gpu(args.app_flags + it, 1u);
+          }
+        }
+      }
+    }
     const int t = (warp >= 8) ? 1 : 0;  // query tile
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -1390,7 +1413,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       float f = -INFINITY;  // frame, base-2 units of the scaled score
       float l = 0.f;
       int nres = 0;
-      float tmax = -INFINITY;  // log2 of the largest P written
+      float pmx = -INFINITY;  // bound on the largest P written
       for (int j = j0; j < e_t; ++j) {
         ok = mbar_wait(bar(kBarSFull + t), sf & 1, abort_flag, &g_prefill_error);
         ++sf;
@@ -1405,8 +1428,8 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         // last visible key of this row, relative to the block
         const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
         // O holds this segment's earlier blocks when j > j0
-        softmax_block<D, BF16, KQ4 != VQ4>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f, l,
-                                           nres, tmax);
+        softmax_block<D, BF16, !(KQ4 && VQ4)>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f,
+                                              l, nres, pmx);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarPReady + t));
@@ -1452,7 +1475,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
             }
           }
           if (store && args.rescale_count) args.rescale_count[orow_idx] = nres;
-          if (store && args.p_max) args.p_max[orow_idx] = ex2(tmax);
+          if (store && args.p_max) args.p_max[orow_idx] = pmx;
           // O has been read out of tensor memory: the next segment's PV may overwrite it
           tc_fence_before();
           mbar_arrive(bar(kBarOFree + t));
@@ -1460,7 +1483,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       } else {
         ok = piece_epilogue<D, BF16>(args.W, args.n_ctas, args.part, args.pflags, args.tag,
                                      args.rescale_count, args.p_max, args.o, args.Hq, args.Sq,
-                                     segs + sidx, ocol, active, f, l, nres, tmax, bar0, pseg,
+                                     segs + sidx, ocol, active, f, l, nres, pmx, bar0, pseg,
                                      abort_flag, merge_flag);
         ++pseg;
       }

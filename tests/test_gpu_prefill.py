@@ -157,11 +157,11 @@ def test_p_never_exceeds_e10(fa, name, launch):
     """The deferred rescale keeps a row's frame until a block's maximum score outgrows it by the
     10-point margin, so no P the softmax writes exceeds e^10 ("perf(rocm): defer SDPA
     accumulator rescale, stage Q once per block (#2306)", What changed).  fa_fwd_kv_stats
-    reports every row's largest P: it must stay at or below e^10 (up to the rounding of the f32
-    exponent argument, < 2e-4 relative at these score magnitudes).  On the score ramp every row
-    carries its frame through blocks whose maximum climbs ~2 per block, so its largest P comes
-    close to the bound (above e^7 on every row); on N(0,1) data the first block sets the frame
-    and P stays far below it."""
+    reports for every row a bound that is at least its largest P (see fa.h): it must stay at or
+    below e^10 (up to the rounding of the f32 exponent argument, < 2e-4 relative at these score
+    magnitudes).  On the score ramp every row carries its frame through blocks whose maximum
+    climbs ~2 per block, so the bound comes close to e^10 (above e^7 on every row); on N(0,1)
+    data the first block sets the frame and P stays far below it."""
     w = fa_inputs.WORKLOADS[name]
     q, k, v = fa_inputs.make_qkv(w, device="cuda", generate_on_device=True)
     ws = None
