@@ -61,6 +61,14 @@ struct Cfg {
   static constexpr int kStages = (KQ4 && VQ4) ? 3 : (D == 128 ? 4 : 6);
   static constexpr int kRawStages = (KQ4 && VQ4) ? 3 : (kAnyQ4 ? 2 : 0);
   static_assert(KQ4 == VQ4 || kStages % 2 == 0, "mixed formats need an even ring");
+  // dense K and V: the ring is used as kStages / 2 slots of two stages, slot g holding the V
+  // tile of block j and the K tile of block j + 1 (the first slot of a unit or segment: K of
+  // its first block alone), so that the MMA issuer waits for one slot and commits one release
+  // per block step.  Each wait or commit costs the single issuing thread 120-350 clk of its
+  // block period (measured), during which the tensor pipe drains.
+  static constexpr bool kPaired = !kAnyQ4;
+  static constexpr int kSlots = kStages / 2;
+  static_assert(!kPaired || kStages % 2 == 0, "paired ring");
   static constexpr int kNibRow = D / 2;                   // bytes of nibbles per key
   static constexpr int kScaleRow = D / 32 * 2;            // bytes of scales per key
   static constexpr int kRawNib = kBN * kNibRow;
@@ -544,14 +552,50 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       }
       ++n;
     };
-    for (int j = 0; j < nbmax; ++j) {
-      produce(false, j);
-      produce(true, j);
+    // dense K/V: one slot per block step, K tile in its first stage, V tile in its second
+    int pg = 0;  // slots filled
+    auto produce_pair = [&](int kj, int vj) {
+      if (!ok) return;
+      const int p = pg % C::kSlots;
+      if (lane == 0) {
+        if (pg >= C::kSlots)
+          ok = mbar_wait(bar(kBarRingEmpty + p), ((pg / C::kSlots) - 1) & 1, abort_flag,
+                         &g_prefill_error);
+        if (ok) {
+          mbar_arrive_expect_tx(bar(kBarRingFull + p),
+                                ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
+          const uint32_t dst = sbase + C::kOffRing + 2 * p * C::kTileBytes;
+          for (int c = 0; c < D / 64; ++c) {
+            if (kj >= 0)
+              tma_load_3d(dst + c * (kBN * 128), &tm_k, bar(kBarRingFull + p), c * 64, kj * kBN,
+                          b * args.Hkv + g);
+            if (vj >= 0)
+              tma_load_3d(dst + C::kTileBytes + c * (kBN * 128), &tm_v, bar(kBarRingFull + p),
+                          c * 64, vj * kBN, b * args.Hkv + g);
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (ok) ++pg;
+    };
+    if constexpr (C::kPaired) {
+      produce_pair(0, -1);
+      for (int j = 0; j < nbmax; ++j) produce_pair(j + 1 < nbmax ? j + 1 : -1, j);
+    } else {
+      for (int j = 0; j < nbmax; ++j) {
+        produce(false, j);
+        produce(true, j);
+      }
     }
     if (!ok && lane == 0) {
       // let copies already issued land before the CTA's shared memory goes away: the last
       // dense tiles sent into the ring and the last raw q4_0 tiles
       volatile int never = 0;
+      if constexpr (C::kPaired) {
+        for (int i = max(0, pg - C::kSlots); i < pg; ++i)
+          mbar_wait(bar(kBarRingFull + i % C::kSlots), (i / C::kSlots) & 1, &never, nullptr,
+                    kWaitLimitNs);
+      }
       for (int i = max(0, n - C::kStages); i < n; ++i)
         if (!((i & 1) ? VQ4 : KQ4))
           mbar_wait(bar(kBarRingFull + i % C::kStages), (i / C::kStages) & 1, &never, nullptr,
@@ -606,6 +650,38 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       // order: QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage is
       // acquired at the start of the step that first uses it and released after its last use
       // (all in ring order).
+      if constexpr (C::kPaired) {
+        // one slot per step: V(j) in stage 2p + 1, K(j + 1) in stage 2p
+        int gn = 0;
+        auto acquire_g = [&]() -> int {
+          const int p = gn % C::kSlots;
+          if (ok) ok = mbar_wait(bar(kBarRingFull + p), (gn / C::kSlots) & 1, abort_flag,
+                                 &g_prefill_error);
+          tc_fence_after();
+          ++gn;
+          return p;
+        };
+        if (nbmax > 0 && ok) {
+          const int p = acquire_g();
+          if (ok) {
+            if (nbA > 0) issue_qk(0, 2 * p);
+            if (nbB > 0) issue_qk(1, 2 * p);
+            release(p);
+          }
+        }
+        for (int j = 0; j < nbmax && ok; ++j) {
+          const int p = acquire_g();
+          const bool next = j + 1 < nbmax;
+          if (!ok) break;
+          if (j < nbA) issue_pv(0, j, 2 * p + 1, nbA);
+          if (!ok) break;
+          if (next && j + 1 < nbA) issue_qk(0, 2 * p);
+          if (j < nbB) issue_pv(1, j, 2 * p + 1, nbB);
+          if (!ok) break;
+          if (next && j + 1 < nbB) issue_qk(1, 2 * p);
+          release(p);
+        }
+      } else {
       if (nbmax > 0 && ok) {
         const int sK = acquire();
         if (ok) {
@@ -632,6 +708,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           if (j + 1 < nbB) issue_qk(1, sK);
           release(sK);
         }
+      }
       }
       if (!ok) {
         // wait until every MMA issued so far has finished before TMEM is released
@@ -1192,6 +1269,32 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       }
       ++n;
     };
+    // dense K/V: one slot per block step, K tile in its first stage, V tile in its second
+    int pg = 0;  // slots filled
+    auto produce_pair = [&](int kj, int vj) {
+      if (!ok) return;
+      const int p = pg % C::kSlots;
+      if (lane == 0) {
+        if (pg >= C::kSlots)
+          ok = mbar_wait(bar(kBarRingEmpty + p), ((pg / C::kSlots) - 1) & 1, abort_flag,
+                         &g_prefill_error);
+        if (ok) {
+          mbar_arrive_expect_tx(bar(kBarRingFull + p),
+                                ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
+          const uint32_t dst = sbase + C::kOffRing + 2 * p * C::kTileBytes;
+          for (int c = 0; c < D / 64; ++c) {
+            if (kj >= 0)
+              tma_load_3d(dst + c * (kBN * 128), &tm_k, bar(kBarRingFull + p), c * 64, kj * kBN,
+                          b * args.Hkv + g);
+            if (vj >= 0)
+              tma_load_3d(dst + C::kTileBytes + c * (kBN * 128), &tm_v, bar(kBarRingFull + p),
+                          c * 64, vj * kBN, b * args.Hkv + g);
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (ok) ++pg;
+    };
     for (int sidx = 0; sidx < nseg && ok; ++sidx) {
       const SegS sg = segs[sidx];
       const bool hasB = sg.q0A + kBM < args.Sq;
@@ -1211,6 +1314,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if constexpr (C::kPaired) {
+        produce_pair(sg.j0, -1);
+        for (int j = sg.j0; j < sg.j1; ++j) produce_pair(j + 1 < sg.j1 ? j + 1 : -1, j);
+      } else {
       for (int j = sg.j0; j < sg.j1; ++j) {
         if constexpr (KQ4 && VQ4) {
           if (args.app_flags != nullptr && ok && j >= args.app_j_lo &&
@@ -1224,6 +1331,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         produce(false, j);
         produce(true, j);
       }
+      }
     }
     if (!ok && lane == 0) {
       // let copies already issued land before the CTA's shared memory goes away: the last
@@ -1231,6 +1339,11 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       volatile int never = 0;
       if (qn > 0)
         mbar_wait(bar(kBarQFull), (qn - 1) & 1, &never, nullptr, kWaitLimitNs);
+      if constexpr (C::kPaired) {
+        for (int i = max(0, pg - C::kSlots); i < pg; ++i)
+          mbar_wait(bar(kBarRingFull + i % C::kSlots), (i / C::kSlots) & 1, &never, nullptr,
+                    kWaitLimitNs);
+      }
       for (int i = max(0, n - C::kStages); i < n; ++i)
         if (!((i & 1) ? VQ4 : KQ4))
           mbar_wait(bar(kBarRingFull + i % C::kStages), (i / C::kStages) & 1, &never, nullptr,
@@ -1250,6 +1363,15 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       int n = 0;
       int prA = 0, prB = 0;    // P-ready waits per tile before this segment (barrier phases)
       int actA = 0, actB = 0;  // earlier segments in which the tile had blocks
+      int gn = 0;              // paired ring: slots taken
+      auto acquire_g = [&]() -> int {
+        const int p = gn % C::kSlots;
+        if (ok) ok = mbar_wait(bar(kBarRingFull + p), (gn / C::kSlots) & 1, abort_flag,
+                               &g_prefill_error);
+        tc_fence_after();
+        ++gn;
+        return p;
+      };
       auto acquire = [&]() -> int {
         const int s = n % C::kStages;
         if (ok) ok = mbar_wait(bar(kBarRingFull + s), (n / C::kStages) & 1, abort_flag,
@@ -1297,6 +1419,37 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         ok = mbar_wait(bar(kBarQFull), sidx & 1, abort_flag, &g_prefill_error);
         tc_fence_after();
         if (!ok) break;
+        const int pbA = prA - j0, pbB = prB - j0;
+        if constexpr (C::kPaired) {
+          // one slot per step: V(j) in stage 2p + 1, K(j + 1) in stage 2p
+          {
+            const int p = acquire_g();
+            if (!ok) break;
+            if (j0 < eA) issue_qk(0, 2 * p);
+            if (j0 < eB) issue_qk(1, 2 * p);
+            release(p);
+            if (j0 + 1 == j1) mma_commit(bar(kBarQEmpty));
+          }
+          if (j0 < eA && actA > 0)
+            ok = ok && mbar_wait(bar(kBarOFree + 0), (actA - 1) & 1, abort_flag,
+                                 &g_prefill_error);
+          if (j0 < eB && actB > 0)
+            ok = ok && mbar_wait(bar(kBarOFree + 1), (actB - 1) & 1, abort_flag,
+                                 &g_prefill_error);
+          for (int j = j0; j < j1 && ok; ++j) {
+            const int p = acquire_g();
+            const bool next = j + 1 < j1;
+            if (!ok) break;
+            if (j < eA) issue_pv(0, j, 2 * p + 1, j0, eA, pbA);
+            if (!ok) break;
+            if (next && j + 1 < eA) issue_qk(0, 2 * p);
+            if (j < eB) issue_pv(1, j, 2 * p + 1, j0, eB, pbB);
+            if (!ok) break;
+            if (next && j + 1 < eB) issue_qk(1, 2 * p);
+            release(p);
+            if (next && j + 2 == j1) mma_commit(bar(kBarQEmpty));
+          }
+        } else {
         {
           const int sK = acquire();
           if (!ok) break;
@@ -1311,7 +1464,6 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           ok = ok && mbar_wait(bar(kBarOFree + 0), (actA - 1) & 1, abort_flag, &g_prefill_error);
         if (j0 < eB && actB > 0)
           ok = ok && mbar_wait(bar(kBarOFree + 1), (actB - 1) & 1, abort_flag, &g_prefill_error);
-        const int pbA = prA - j0, pbB = prB - j0;
         for (int j = j0; j < j1 && ok; ++j) {
           const int sV = acquire();
           const bool next = j + 1 < j1;
@@ -1328,6 +1480,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
             release(sK);
             if (j + 2 == j1) mma_commit(bar(kBarQEmpty));
           }
+        }
         }
         if (j0 < eA) {
           ++actA;
