@@ -65,7 +65,10 @@ struct Cfg {
   // tile of block j and the K tile of block j + 1 (the first slot of a unit or segment: K of
   // its first block alone), so that the MMA issuer waits for one slot and commits one release
   // per block step.  Each wait or commit costs the single issuing thread 120-350 clk of its
-  // block period (measured), during which the tensor pipe drains.
+  // block period (measured), during which the tensor pipe drains.  A slot whose K tile tile B
+  // multiplies is released by tile B's softmax on seeing that QK complete (the issuer's commit
+  // covers every MMA it issued before, so also the earlier reads of the slot); the issuer
+  // commits the release only of the others.
   static constexpr bool kPaired = !kAnyQ4;
   static constexpr int kSlots = kStages / 2;
   static_assert(!kPaired || kStages % 2 == 0, "paired ring");
@@ -665,8 +668,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           const int p = acquire_g();
           if (ok) {
             if (nbA > 0) issue_qk(0, 2 * p);
-            if (nbB > 0) issue_qk(1, 2 * p);
-            release(p);
+            if (nbB > 0)
+              issue_qk(1, 2 * p);  // tile B's softmax releases the slot
+            else
+              release(p);
           }
         }
         for (int j = 0; j < nbmax && ok; ++j) {
@@ -678,8 +683,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           if (next && j + 1 < nbA) issue_qk(0, 2 * p);
           if (j < nbB) issue_pv(1, j, 2 * p + 1, nbB);
           if (!ok) break;
-          if (next && j + 1 < nbB) issue_qk(1, 2 * p);
-          release(p);
+          if (next && j + 1 < nbB)
+            issue_qk(1, 2 * p);
+          else
+            release(p);
         }
       } else {
       if (nbmax > 0 && ok) {
@@ -741,6 +748,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         break;
       }
       tc_fence_after();
+      if constexpr (C::kPaired) {
+        // QK_B of block j done: release the ring slot holding K(j) (slot j of the unit)
+        if (t == 1 && warp == 8 && lane == 0) mbar_arrive(bar(kBarRingEmpty + j % C::kSlots));
+      }
       const int kb = j * kBN;
       const bool need_mask =
           (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
@@ -1426,8 +1437,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
             const int p = acquire_g();
             if (!ok) break;
             if (j0 < eA) issue_qk(0, 2 * p);
-            if (j0 < eB) issue_qk(1, 2 * p);
-            release(p);
+            if (j0 < eB)
+              issue_qk(1, 2 * p);  // tile B's softmax releases the slot
+            else
+              release(p);
             if (j0 + 1 == j1) mma_commit(bar(kBarQEmpty));
           }
           if (j0 < eA && actA > 0)
@@ -1445,8 +1458,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
             if (next && j + 1 < eA) issue_qk(0, 2 * p);
             if (j < eB) issue_pv(1, j, 2 * p + 1, j0, eB, pbB);
             if (!ok) break;
-            if (next && j + 1 < eB) issue_qk(1, 2 * p);
-            release(p);
+            if (next && j + 1 < eB)
+              issue_qk(1, 2 * p);
+            else
+              release(p);
             if (next && j + 2 == j1) mma_commit(bar(kBarQEmpty));
           }
         } else {
@@ -1557,9 +1572,12 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
     int sf = 0;    // S-full waits so far (barrier phase)
     int od = 0;    // segments in which this tile had blocks (O-done phase)
     int pseg = 0;  // pieces published so far
+    int gn = 0;    // paired ring: slots of the segments before this one
     for (int sidx = 0; sidx < nseg && ok; ++sidx) {
       // only what the block loop needs is read before it; the rest after it
       const int j0 = segs[sidx].j0;
+      const int g0 = gn - j0;  // ring slot of the one holding K(j): g0 + j
+      gn += segs[sidx].j1 - j0 + 1;
       const int q0 = segs[sidx].q0A + t * kBM;
       const int e_t = q0 < args.Sq ? min(segs[sidx].j1, t ? segs[sidx].nbB : segs[sidx].nbA) : 0;
       const int pos = args.q_pos_offset + q0 + row;
@@ -1575,6 +1593,11 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           break;
         }
         tc_fence_after();
+        if constexpr (C::kPaired) {
+          // QK_B of block j done: release the ring slot holding K(j)
+          if (t == 1 && warp == 8 && lane == 0)
+            mbar_arrive(bar(kBarRingEmpty + (g0 + j) % C::kSlots));
+        }
         const int kb = j * kBN;
         const bool need_mask =
             (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
