@@ -51,7 +51,8 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM column of the S block of query tile t (0: A, 1: B); P overwrites its first half
 __host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
 
-template <int D, bool KQ4, bool VQ4>
+// WIDE: the sixteen-warp layout with q4_0 K or V (the cut-schedule kernel)
+template <int D, bool KQ4, bool VQ4, bool WIDE = false>
 struct Cfg {
   static constexpr bool kAnyQ4 = KQ4 || VQ4;
   static constexpr int kTileBytes = kBN * D * 2;          // one f16/bf16 K or V tile
@@ -82,7 +83,21 @@ struct Cfg {
   static constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
   static constexpr int kBarBytes = 512 + 1024;  // barriers, flags, then the segment table
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
-  static constexpr int kWarps = 12;
+  // warps: 0 producer, 1 MMA issuer, 4-11 softmax (one thread per query row), 2-3 dequant
+  // with q4_0 K or V; WIDE adds dequant warps 12-15 (sixteen warps, so 128 registers a thread:
+  // the softmax then takes its two-pass form).  Measured at 16K keys, q4_0 K and V: the cut
+  // kernel's step is bound by the dequant warps' rate, 0.477 -> 0.440 ms with six of them;
+  // the one-unit kernel loses more to the two-pass softmax than it gains.
+  static constexpr bool kWide = WIDE && kAnyQ4;
+  static constexpr int kDqWarps = kAnyQ4 ? (kWide ? 6 : 2) : 0;
+  static constexpr int kDqThreads = kDqWarps * 32;
+  static constexpr int kWarps = kWide ? 16 : 12;
+  static __device__ __forceinline__ bool is_dq_warp(int w) {
+    return w == 2 || w == 3 || (kWide && w >= 12);
+  }
+  static __device__ __forceinline__ int dq_index(int w, int lane) {
+    return (w < 4 ? w - 2 : w - 10) * 32 + lane;
+  }
   static constexpr int kThreads = kWarps * 32;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;     // O of tile A / B
 };
@@ -417,6 +432,49 @@ __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool
   }
 }
 
+// One q4_0 dequant item: the 32 elements of block blk of key row t of a raw tile (nibble rows of
+// NIB bytes, 64B-swizzled at D = 128 and 32B-swizzled at D = 64, then the fp16 scale rows of SROW
+// bytes from byte RAWNIB), expanded to (q - 8) * d in f16/bf16 into the 128B-swizzled ring stage.
+template <int D, bool BF16, int NIB, int SROW, int RAWNIB>
+__device__ __forceinline__ void dequant_item(const uint8_t* raw, uint8_t* dst, int t, int blk,
+                                             uint32_t mg) {
+  const uint8_t* nrow = raw + t * NIB;
+  const __half* srow = reinterpret_cast<const __half*>(raw + RAWNIB + t * SROW);
+    // 16 bytes of nibbles of this key, 64B-swizzled (D=128) or 32B-swizzled (D=64)
+    const int chunk = (D == 128) ? (blk ^ ((t >> 1) & 3)) : (blk ^ ((t >> 2) & 1));
+    const uint4 wv = *reinterpret_cast<const uint4*>(nrow + 16 * chunk);
+    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+    const __half dh = srow[blk];
+    uint32_t outv[16];  // 32 dequantized elements, packed in pairs, natural order
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      // bytes 4q..4q+3 -> elements 4q..4q+3 (low) and 4q+16..4q+19 (high)
+      const uint32_t a = __byte_perm(w[q], 0u, 0x5150);   // byte0 at b0, byte1 at b2
+      const uint32_t c2 = __byte_perm(w[q], 0u, 0x5352);  // byte2 at b0, byte3 at b2
+      if (BF16) {
+        const float d = __half2float(dh);
+        outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a, mg), d);
+        outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2, mg), d);
+        outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a, mg), d);
+        outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2, mg), d);
+      } else {
+        outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a, mg), dh);
+        outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2, mg), dh);
+        outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a, mg), dh);
+        outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2, mg), dh);
+      }
+    }
+    // elements 32 blk + 8 cc .. +7 form 16-byte chunk (4 blk + cc) of the row
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const int col16 = 4 * blk + cc;        // 16-byte chunk index along D
+      const int atom = col16 >> 3;           // 64-element swizzle atom
+      const int ch = (col16 & 7) ^ (t & 7);  // 128B swizzle
+      *reinterpret_cast<uint4*>(dst + atom * (kBN * 128) + t * 128 + ch * 16) =
+          make_uint4(outv[4 * cc], outv[4 * cc + 1], outv[4 * cc + 2], outv[4 * cc + 3]);
+    }
+}
+
 // number of 128-key blocks a query tile starting at row q0 must visit
 __host__ __device__ __forceinline__ int tile_blocks(const PrefillArgs& a, int q0) {
   if (q0 >= a.Sq) return 0;
@@ -464,14 +522,14 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
     }
     mbar_init(bar(kBarDrain), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      // a q4_0 stage is filled by the 64 dequant threads, a dense one by the TMA lane
+      // a q4_0 stage is filled by the dequant threads, a dense one by the TMA lane
       const bool q4s = (C::kStages % 2 == 0) ? ((s & 1) ? VQ4 : KQ4) : (KQ4 && VQ4);
-      mbar_init(bar(kBarRingFull + s), q4s ? 64 : 1);
+      mbar_init(bar(kBarRingFull + s), q4s ? C::kDqThreads : 1);
       mbar_init(bar(kBarRingEmpty + s), 1);
     }
     for (int s = 0; s < C::kRawStages; ++s) {
       mbar_init(bar(kBarRawFull + s), 1 + 32);  // TMA lane + 32 cp.async arrivals
-      mbar_init(bar(kBarRawEmpty + s), 64);
+      mbar_init(bar(kBarRawEmpty + s), C::kDqThreads);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -798,11 +856,11 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         args.p_max[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = pmx;
     }
   } else if constexpr (C::kAnyQ4) {
-    if (warp == 2 || warp == 3) {
+    if (C::is_dq_warp(warp)) {
       // -------------------------------------------------------------- q4_0 dequant
-      // thread u expands key rows u and u + 64 of each raw tile into the 128B-swizzled
-      // f16/bf16 ring stage
-      const int u = threadIdx.x - 2 * 32;
+      // the dequant threads share out each raw tile's (key row, block) items and expand them
+      // into the 128B-swizzled f16/bf16 ring stage
+      const int u = C::dq_index(warp, lane);
       const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
       bool ok = true;
       const int ntiles = 2 * nbmax;
@@ -819,48 +877,15 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         if (!ok) break;
         const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
         uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
-#pragma unroll 1
-        for (int rr = 0; rr < 2; ++rr) {
-        const int t = u + 64 * rr;  // key row within the tile
-        const uint8_t* nrow = raw + t * C::kNibRow;
-        const __half* srow =
-            reinterpret_cast<const __half*>(raw + C::kRawNib + t * C::kScaleRow);
+        // items (key row t, 32-element block blk) of the tile, rows fastest; unrolled so that
+        // the items' shared-memory loads overlap
+        constexpr int kItems = kBN * (D / 32);
 #pragma unroll
-        for (int blk = 0; blk < D / 32; ++blk) {
-          // 16 bytes of nibbles of this key, 64B-swizzled (D=128) or 32B-swizzled (D=64)
-          const int chunk = (D == 128) ? (blk ^ ((t >> 1) & 3)) : (blk ^ ((t >> 2) & 1));
-          const uint4 wv = *reinterpret_cast<const uint4*>(nrow + 16 * chunk);
-          const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-          const __half dh = srow[blk];
-          uint32_t outv[16];  // 32 dequantized elements, packed in pairs, natural order
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            // bytes 4q..4q+3 -> elements 4q..4q+3 (low) and 4q+16..4q+19 (high)
-            const uint32_t a = __byte_perm(w[q], 0u, 0x5150);   // byte0 at b0, byte1 at b2
-            const uint32_t c2 = __byte_perm(w[q], 0u, 0x5352);  // byte2 at b0, byte3 at b2
-            if (BF16) {
-              const float d = __half2float(dh);
-              outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a, mg), d);
-              outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2, mg), d);
-              outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a, mg), d);
-              outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2, mg), d);
-            } else {
-              outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a, mg), dh);
-              outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2, mg), dh);
-              outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a, mg), dh);
-              outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2, mg), dh);
-            }
-          }
-          // elements 32 blk + 8 cc .. +7 form 16-byte chunk (4 blk + cc) of the row
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int col16 = 4 * blk + cc;        // 16-byte chunk index along D
-            const int atom = col16 >> 3;           // 64-element swizzle atom
-            const int ch = (col16 & 7) ^ (t & 7);  // 128B swizzle
-            *reinterpret_cast<uint4*>(dst + atom * (kBN * 128) + t * 128 + ch * 16) =
-                make_uint4(outv[4 * cc], outv[4 * cc + 1], outv[4 * cc + 2], outv[4 * cc + 3]);
-          }
-        }
+        for (int k = 0; k < (kItems + C::kDqThreads - 1) / C::kDqThreads; ++k) {
+          const int it = u + k * C::kDqThreads;
+          if (kItems % C::kDqThreads == 0 || it < kItems)
+            dequant_item<D, BF16, C::kNibRow, C::kScaleRow, C::kRawNib>(raw, dst, it % kBN,
+                                                                        it / kBN, mg);
         }
         // generic-proxy writes must be visible to the tensor core's async proxy
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1146,11 +1171,11 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
 // long units).
 // ------------------------------------------------------------------------------------------
 template <int D, bool BF16, bool KQ4, bool VQ4>
-__global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
     prefill_seg_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
-  using C = Cfg<D, KQ4, VQ4>;
+  using C = Cfg<D, KQ4, VQ4, true>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -1186,14 +1211,14 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
     mbar_init(bar(kBarPiece), 256);
     mbar_init(bar(kBarMergeDecided), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      // a q4_0 stage is filled by the 64 dequant threads, a dense one by the TMA lane
+      // a q4_0 stage is filled by the dequant threads, a dense one by the TMA lane
       const bool q4s = (C::kStages % 2 == 0) ? ((s & 1) ? VQ4 : KQ4) : (KQ4 && VQ4);
-      mbar_init(bar(kBarRingFull + s), q4s ? 64 : 1);
+      mbar_init(bar(kBarRingFull + s), q4s ? C::kDqThreads : 1);
       mbar_init(bar(kBarRingEmpty + s), 1);
     }
     for (int s = 0; s < C::kRawStages; ++s) {
       mbar_init(bar(kBarRawFull + s), 1 + 32);  // TMA lane + 32 cp.async arrivals
-      mbar_init(bar(kBarRawEmpty + s), 64);
+      mbar_init(bar(kBarRawEmpty + s), C::kDqThreads);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -1604,7 +1629,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         // last visible key of this row, relative to the block
         const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
         // O holds this segment's earlier blocks when j > j0
-        softmax_block<D, BF16, !(KQ4 && VQ4)>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f,
+        softmax_block<D, BF16, !C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f,
                                               l, nres, pmx);
         tmem_wait_st();
         tc_fence_before();
@@ -1665,11 +1690,11 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
       }
     }
   } else if constexpr (C::kAnyQ4) {
-    if (warp == 2 || warp == 3) {
+    if (C::is_dq_warp(warp)) {
       // -------------------------------------------------------------- q4_0 dequant
-      // thread u expands key rows u and u + 64 of each raw tile into the 128B-swizzled
-      // f16/bf16 ring stage
-      const int u = threadIdx.x - 2 * 32;
+      // the dequant threads share out each raw tile's (key row, block) items and expand them
+      // into the 128B-swizzled f16/bf16 ring stage
+      const int u = C::dq_index(warp, lane);
       const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
       bool ok = true;
       const int ntiles = static_cast<int>(2 * (t_end - t_begin));  // K and V of every step
@@ -1686,48 +1711,15 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
         if (!ok) break;
         const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
         uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
-#pragma unroll 1
-        for (int rr = 0; rr < 2; ++rr) {
-        const int t = u + 64 * rr;  // key row within the tile
-        const uint8_t* nrow = raw + t * C::kNibRow;
-        const __half* srow =
-            reinterpret_cast<const __half*>(raw + C::kRawNib + t * C::kScaleRow);
+        // items (key row t, 32-element block blk) of the tile, rows fastest; unrolled so that
+        // the items' shared-memory loads overlap
+        constexpr int kItems = kBN * (D / 32);
 #pragma unroll
-        for (int blk = 0; blk < D / 32; ++blk) {
-          // 16 bytes of nibbles of this key, 64B-swizzled (D=128) or 32B-swizzled (D=64)
-          const int chunk = (D == 128) ? (blk ^ ((t >> 1) & 3)) : (blk ^ ((t >> 2) & 1));
-          const uint4 wv = *reinterpret_cast<const uint4*>(nrow + 16 * chunk);
-          const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-          const __half dh = srow[blk];
-          uint32_t outv[16];  // 32 dequantized elements, packed in pairs, natural order
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            // bytes 4q..4q+3 -> elements 4q..4q+3 (low) and 4q+16..4q+19 (high)
-            const uint32_t a = __byte_perm(w[q], 0u, 0x5150);   // byte0 at b0, byte1 at b2
-            const uint32_t c2 = __byte_perm(w[q], 0u, 0x5352);  // byte2 at b0, byte3 at b2
-            if (BF16) {
-              const float d = __half2float(dh);
-              outv[2 * q + 0] = Dq<true>::scale(Dq<true>::lo(a, mg), d);
-              outv[2 * q + 1] = Dq<true>::scale(Dq<true>::lo(c2, mg), d);
-              outv[8 + 2 * q + 0] = Dq<true>::scale(Dq<true>::hi(a, mg), d);
-              outv[8 + 2 * q + 1] = Dq<true>::scale(Dq<true>::hi(c2, mg), d);
-            } else {
-              outv[2 * q + 0] = Dq<false>::scale(Dq<false>::lo(a, mg), dh);
-              outv[2 * q + 1] = Dq<false>::scale(Dq<false>::lo(c2, mg), dh);
-              outv[8 + 2 * q + 0] = Dq<false>::scale(Dq<false>::hi(a, mg), dh);
-              outv[8 + 2 * q + 1] = Dq<false>::scale(Dq<false>::hi(c2, mg), dh);
-            }
-          }
-          // elements 32 blk + 8 cc .. +7 form 16-byte chunk (4 blk + cc) of the row
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int col16 = 4 * blk + cc;        // 16-byte chunk index along D
-            const int atom = col16 >> 3;           // 64-element swizzle atom
-            const int ch = (col16 & 7) ^ (t & 7);  // 128B swizzle
-            *reinterpret_cast<uint4*>(dst + atom * (kBN * 128) + t * 128 + ch * 16) =
-                make_uint4(outv[4 * cc], outv[4 * cc + 1], outv[4 * cc + 2], outv[4 * cc + 3]);
-          }
-        }
+        for (int k = 0; k < (kItems + C::kDqThreads - 1) / C::kDqThreads; ++k) {
+          const int it = u + k * C::kDqThreads;
+          if (kItems % C::kDqThreads == 0 || it < kItems)
+            dequant_item<D, BF16, C::kNibRow, C::kScaleRow, C::kRawNib>(raw, dst, it % kBN,
+                                                                        it / kBN, mg);
         }
         // generic-proxy writes must be visible to the tensor core's async proxy
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1910,7 +1902,7 @@ static cudaError_t launch_fmt(const PrefillLaunch& L, cudaStream_t stream) {
 // equal cuts of the step sequence over one CTA per SM (D = 128, any pair of K/V formats)
 template <bool BF16, bool KQ4, bool VQ4>
 static cudaError_t launch_seg(const PrefillLaunch& L, const Plan& p, cudaStream_t stream) {
-  using C = Cfg<128, KQ4, VQ4>;
+  using C = Cfg<128, KQ4, VQ4, true>;
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
   auto kern = prefill_seg_kernel<128, BF16, KQ4, VQ4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1969,7 +1961,7 @@ size_t prefill_append_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, in
 template <bool BF16>
 static cudaError_t launch_seg_append(const PrefillLaunch& L, const PrefillAppend& A,
                                      const Plan& p, cudaStream_t stream) {
-  using C = Cfg<128, true, true>;
+  using C = Cfg<128, true, true, true>;
   auto kern = prefill_seg_kernel<128, BF16, true, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
