@@ -344,6 +344,50 @@ __device__ __forceinline__ float row_max_regs(const float (&s)[kBN]) {
 // of the exponential cannot hide a P at the bound.
 constexpr float kSumTrigger = 21800.f;
 
+// Single read of S(j) in 32-key chunks (one TMEM wait each) for kernels with 128 registers a
+// thread: P = 2^(s * sl2 + nf) in the current frame, kept packed in registers (64 of them) until
+// the warp knows that no row's sum exceeds kSumTrigger; then P is stored over S's first half,
+// its row sum goes to sum and the result is true.  Otherwise nothing is stored (S(j) is intact)
+// and the result is false.
+template <bool MASK, bool BF16>
+__device__ __forceinline__ bool block_row_p_chunked(uint32_t scol, int rel_lim, float sl2,
+                                                    float nf, float& sum) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), nfx2 = f2_pack(nf, nf);
+  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+  uint32_t pr[kBN / 2];
+#pragma unroll
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(scol + 32 * c, r);
+    tmem_wait_ld();
+    reg_fence32(r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+      if (MASK) {
+        if (32 * c + 2 * i > rel_lim) s0 = -INFINITY;
+        if (32 * c + 2 * i + 1 > rel_lim) s1 = -INFINITY;
+      }
+      const float2 t = f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, nfx2));
+      const float p0 = ex2(t.x), p1 = ex2(t.y);
+      const uint64_t pp = f2_pack(p0, p1);
+      if (i & 1) acc1 = f2_add(acc1, pp); else acc0 = f2_add(acc0, pp);
+      pr[16 * c + i] = pack2<BF16>(p0, p1);
+    }
+  }
+  const float2 a = f2_unpack(f2_add(acc0, acc1));
+  sum = a.x + a.y;
+  if (__any_sync(0xffffffffu, sum > kSumTrigger)) return false;
+#pragma unroll
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = pr[16 * c + i];
+    tmem_st16(scol + 16 * c, q);
+  }
+  return true;
+}
+
 // One key block of the online softmax for this thread's query row: read S(j), move the frame f
 // to the block max when that exceeds f by more than the margin (l and, when it already holds
 // earlier blocks (o_live), O are scaled by 2^(f_old - f)), write P = 2^(s - f) over S and add
@@ -360,7 +404,7 @@ constexpr float kSumTrigger = 21800.f;
 // frame in force for its block: the exact largest P of a block that ran the frame test (P is
 // monotonic in the score), the block's sum of P otherwise (at least its largest P, and below
 // kSumTrigger).  Either way pmx <= e^10 whenever the frame rule holds.
-template <int D, bool BF16, bool ONE_READ>
+template <int D, bool BF16, bool ONE_READ, bool CHUNKED = false>
 __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool need_mask,
                                               int rel_lim, float sl2, bool o_live, float& f,
                                               float& l, int& nres, float& pmx) {
@@ -417,6 +461,20 @@ __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool
     }
     l += sum;
   } else {
+    if constexpr (CHUNKED) {
+      // the chunked single read first (not on a row's first block, whose frame is unset)
+      if (!__any_sync(0xffffffffu, f == -INFINITY)) {
+        float sum;
+        const bool done = need_mask ? block_row_p_chunked<true, BF16>(scol, rel_lim, sl2, -f, sum)
+                                    : block_row_p_chunked<false, BF16>(scol, rel_lim, sl2, -f,
+                                                                       sum);
+        if (done) {
+          pmx = fmaxf(pmx, sum);
+          l += sum;
+          return;
+        }
+      }
+    }
     // two passes over S in tensor memory: the row max (and the frame test) first, then P
     const float mx = need_mask ? block_row_max<true>(scol, rel_lim)
                                : block_row_max<false>(scol, rel_lim);
@@ -1629,7 +1687,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
         // last visible key of this row, relative to the block
         const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
         // O holds this segment's earlier blocks when j > j0
-        softmax_block<D, BF16, !C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f,
+        softmax_block<D, BF16, !C::kWide, C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f,
                                               l, nres, pmx);
         tmem_wait_st();
         tc_fence_before();
