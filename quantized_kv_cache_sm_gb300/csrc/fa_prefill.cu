@@ -51,7 +51,7 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM column of the S block of query tile t (0: A, 1: B); P overwrites its first half
 __host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
 
-// WIDE: the sixteen-warp layout with q4_0 K or V (the cut-schedule kernel)
+// WIDE: the sixteen-warp layout with q4_0 K or V (both prefill kernels use it)
 template <int D, bool KQ4, bool VQ4, bool WIDE = false>
 struct Cfg {
   static constexpr bool kAnyQ4 = KQ4 || VQ4;
@@ -85,9 +85,9 @@ struct Cfg {
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   // warps: 0 producer, 1 MMA issuer, 4-11 softmax (one thread per query row), 2-3 dequant
   // with q4_0 K or V; WIDE adds dequant warps 12-15 (sixteen warps, so 128 registers a thread:
-  // the softmax then takes its two-pass form).  Measured at 16K keys, q4_0 K and V: the cut
-  // kernel's step is bound by the dequant warps' rate, 0.477 -> 0.440 ms with six of them;
-  // the one-unit kernel loses more to the two-pass softmax than it gains.
+  // the softmax then reads S in 32-key chunks).  Measured at 16K keys, q4_0 K and V: with two
+  // dequant warps the step waits for dequantized tiles; six of them and the chunked read take
+  // the cut kernel from 0.477 to 0.410 ms and the one-unit kernel from 0.484 to 0.443 ms.
   static constexpr bool kWide = WIDE && kAnyQ4;
   static constexpr int kDqWarps = kAnyQ4 ? (kWide ? 6 : 2) : 0;
   static constexpr int kDqThreads = kDqWarps * 32;
@@ -542,11 +542,11 @@ __host__ __device__ __forceinline__ int tile_blocks(const PrefillArgs& a, int q0
 }
 
 template <int D, bool BF16, bool KQ4, bool VQ4>
-__global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs args) {
-  using C = Cfg<D, KQ4, VQ4>;
+  using C = Cfg<D, KQ4, VQ4, true>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -873,8 +873,8 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4>::kThreads, 1)
           (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
       // last visible key of this row, relative to the block
       const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
-      softmax_block<D, BF16, true>(scol, ocol, need_mask, rel_lim, sl2, j > 0, f, l, nres,
-                                   pmx);
+      softmax_block<D, BF16, !C::kWide, C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > 0, f,
+                                                  l, nres, pmx);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPReady + t));
@@ -1916,7 +1916,7 @@ int64_t prefill_debug_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int q_pos
 
 template <int D, bool BF16, bool KQ4, bool VQ4>
 static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
-  using C = Cfg<D, KQ4, VQ4>;
+  using C = Cfg<D, KQ4, VQ4, true>;
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
   auto kern = prefill_kernel<D, BF16, KQ4, VQ4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
