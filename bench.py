@@ -90,6 +90,26 @@ def kv_bytes_q4_0(w: fa_inputs.Workload) -> int:
     return 2 * w.B * w.Hkv * keys * per_row
 
 
+def kv_bytes(w: fa_inputs.Workload) -> int:
+    """Algorithmic K+V bytes one call of a decode workload reads (q4_0 or 16-bit cache)."""
+    if w.kv_format == "q4_0":
+        return kv_bytes_q4_0(w)
+    keys = (w.q_pos_offset + 1) if w.causal else w.Sk
+    return 2 * w.B * w.Hkv * keys * w.D * 2
+
+
+def is_decode(w: fa_inputs.Workload) -> bool:
+    return w.Sq == 1
+
+
+def rate(w: fa_inputs.Workload, ms: float, share: float = 1.0):
+    """The workload's metric for `share` of one call taking `ms`: KV GB/s for a decode workload
+    (bound by HBM), TFLOP/s otherwise (bound by the tensor cores)."""
+    if is_decode(w):
+        return kv_bytes(w) * share / (ms * 1e-3) / 1e9, "GB/s"
+    return w.flops() * share / (ms * 1e-3) / 1e12, "TFLOP/s"
+
+
 def aggregate(local_ms: float, world: int) -> float:
     """Max over ranks of a per-rank time (ms); identity without a process group."""
     import torch.distributed as dist
@@ -211,7 +231,10 @@ def run_ours(args, rank, world, local_rank):
     # library plans one for this device; without it the prefill runs one work unit per CTA
     n_ws = fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset, w.causal)
     ws = torch.empty(n_ws, dtype=torch.uint8, device=dev) if n_ws > 0 else None
-    kernel = "prefill_seg_kernel" if w.Sq > 1 and n_ws > 0 and w.D == 128 else "prefill_kernel"
+    if is_decode(w):
+        kernel = "decode_split_kernel"
+    else:
+        kernel = "prefill_seg_kernel" if n_ws > 0 and w.D == 128 else "prefill_kernel"
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -249,13 +272,21 @@ def run_ours(args, rank, world, local_rank):
     assert status == fa.FA_OK, fa.status_name(status)
 
     flops = w.flops()
-    value = flops * world / (ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]  # f16 and bf16 share the dense tensor rate
-    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    value, unit = rate(w, ms, world)
+    achieved, _ = rate(w, kernel_ms)
+    if is_decode(w):
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "peak_source": f"{peaks_src} HBM copy",
+                "algorithmic_bytes_per_launch": kv_bytes(w)}
+    else:
+        peak = peaks["bf16_tflops"]  # f16 and bf16 share the dense tensor rate
+        roof = {"bound": "tensor",
+                "peak_source": f"{peaks_src} bf16 dense burst (f16 runs at the same rate)",
+                "algorithmic_flops_per_launch": flops}
     line = {
         "metric": METRIC,
         "value": round(value, 2),
-        "unit": "TFLOP/s",
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -275,15 +306,15 @@ def run_ours(args, rank, world, local_rank):
         },
         "roofline": {
             "kernel": kernel,
-            "bound": "tensor",
+            "bound": roof["bound"],
             "achieved": round(achieved, 2),
             "peak": peak,
-            "unit": "TFLOP/s",
+            "unit": unit,
             "frac": round(achieved / peak, 4),
-            "peak_source": f"{peaks_src} bf16 dense burst (f16 runs at the same rate)",
+            "peak_source": roof["peak_source"],
             "traffic": measured_traffic(f"{kernel}_{w.dtype}_{w.kv_format}", w.name),
             "traffic_unit": "bytes per launch (ncu dram read + write)",
-            "algorithmic_flops_per_launch": flops,
+            **{k: v for k, v in roof.items() if k.startswith("algorithmic")},
         },
         "gpu_launches": args.steps,
         "clocks": clocks,
@@ -358,12 +389,13 @@ def e2e_leg(fa, w, dev, stream, steps, warmup, world):
     ms = aggregate(span(steps) / steps, world)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = q.numel() * q.element_size()
-    tflops = lambda t: round(w.flops() * world / (t * 1e-3) / 1e12, 2)
-    return {"value": tflops(ms), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+    unit = rate(w, 1.0)[1]
+    tflops = lambda t: round(rate(w, t, world)[0], 2)
+    return {"value": tflops(ms), "unit": unit, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "overlap": "steps alternate between two streams: step i+1's host-to-device copies "
                        "overlap step i's kernel and read-back",
-            "sequential": {"value": tflops(seq_ms), "unit": "TFLOP/s",
+            "sequential": {"value": tflops(seq_ms), "unit": unit,
                            "ms_per_step": round(seq_ms, 4)}}
 
 
@@ -611,7 +643,8 @@ def cpu_baseline(w, budget_s=15.0):
     _oracle_call(w, qn, kv, rows, threads)
     dt = time.perf_counter() - t0
     fl = _rows_flops(w, rows)
-    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+    value, unit = (rate(w, dt * 1e3, nrows / n) if is_decode(w) else (fl / dt / 1e12, "TFLOP/s"))
+    return {"value": round(value, 6), "unit": unit, "cores": threads,
             "kind": "oracle",
             "sample": f"{nrows} random query rows of {w.name} (of {n}), all their visible keys, "
                       f"f64, {dt:.1f} s wall",
@@ -647,20 +680,22 @@ def run_reference(args, rank, world):
         _oracle_call(w, qn, kv, rows, threads)
         tot_t += time.perf_counter() - t0
         tot_fl += _rows_flops(w, rows)
-    value = tot_fl / tot_t / 1e12
+    # a decode workload: the share of the call's KV bytes behind the sampled query rows
+    value, unit = (rate(w, tot_t * 1e3 / args.steps, rows_per_step / n) if is_decode(w)
+                   else (tot_fl / tot_t / 1e12, "TFLOP/s"))
     sample = (f"{rows_per_step} random query rows of {w.name} per step (of {n}), all their "
               f"visible keys, f64")
     return {
-        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq,
                    "Sk": w.Sk, "D": w.D, "kv_format": w.kv_format,
                    "sample_rows_per_step": rows_per_step},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads,
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 

@@ -19,6 +19,18 @@ def test_decode_kv_bytes():
     assert bench.kv_bytes_q4_0(w) == 301_989_888
 
 
+def test_decode_workloads_report_kv_bandwidth():
+    w = fa_inputs.WORKLOADS["decode_q4_0_b4_gqa32x8_d128_sk65536_f16"]
+    # 301 989 888 bytes in 0.06 ms: 5033.2 GB/s; a quarter of the rows: a quarter of the bytes
+    v, unit = bench.rate(w, 0.06)
+    assert unit == "GB/s" and abs(v - 301_989_888 / 0.06e-3 / 1e9) < 1e-6
+    assert abs(bench.rate(w, 0.06, 0.25)[0] - v / 4) < 1e-6
+    p = fa_inputs.WORKLOADS["prefill_gqa32x8_d128_sq2048_sk16384_f16"]
+    v, unit = bench.rate(p, 0.5)
+    assert unit == "TFLOP/s" and abs(v - p.flops() / 0.5e-3 / 1e12) < 1e-9
+    assert not bench.is_decode(p) and bench.is_decode(w)
+
+
 def test_parse_clocks():
     lines = [
         "0, 1965, 2070, 1012.3, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
