@@ -1186,29 +1186,34 @@ __device__ __noinline__ bool piece_epilogue(int64_t W, int n_ctas, float* part,
       T = fmaxf(T, __ldcg(pc + (D + 3) * kBM));
     }
     const float inv_l = 1.f / L;
+    // half a row (D/2 columns) of every piece in turn, all of a piece's loads issued together:
+    // one L2 round trip per piece and half row, not one per piece and 16 columns
+    constexpr int kH = D / 2;
 #pragma unroll 1
-    for (int cc = 0; cc < D / 16; ++cc) {
-      float acc[16];
+    for (int h2 = 0; h2 < 2; ++h2) {
+      float acc[kH];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+      for (int i = 0; i < kH; ++i) acc[i] = 0.f;
       for (int c = c_first; c <= c_last; ++c) {
         const float* pc = tile_of(c);
         const float fp = __ldcg(pc + D * kBM);
+        float v[kH];
+#pragma unroll
+        for (int i = 0; i < kH; ++i) v[i] = __ldcg(pc + (kH * h2 + i) * kBM);
         if (fp == -INFINITY) continue;
         const float w = ex2(fp - F);
-        float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __ldcg(pc + (16 * cc + i) * kBM);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+        for (int i = 0; i < kH; ++i) acc[i] = fmaf(w, v[i], acc[i]);
       }
-      uint32_t pk[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) pk[i] = pack2<BF16>(acc[2 * i] * inv_l, acc[2 * i + 1] * inv_l);
       if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+        for (int cc = 0; cc < kH / 8; ++cc) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            pk[i] = pack2<BF16>(acc[8 * cc + 2 * i] * inv_l, acc[8 * cc + 2 * i + 1] * inv_l);
+          reinterpret_cast<uint4*>(orow + kH * 2 * h2)[cc] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       }
     }
     if (store && rescale_count) rescale_count[orow_idx] = moves;
