@@ -234,6 +234,20 @@ __host__ __device__ __forceinline__ bool paged_slot(const int32_t* seq_lens, int
   }
   return false;
 }
+// Uniform batch: split s of ns over `len` keys in tiles of `tile` keys.  The tiles are shared out
+// as evenly as whole tiles allow, the longer splits first: every CTA of the launch then does the
+// same work to within one tile, and with the grid's split index slowest the CTAs dispatched
+// last onto each SM (the highest splits) get the shorter ranges (measured: 64.1 -> 62.3 us at 4 x
+// 65 536 keys, against equal chunks with a short last one and the split index fastest).
+__host__ __device__ __forceinline__ void uniform_split(int s, int ns, int len, int tile, int& kb0,
+                                                       int& kb1) {
+  const int tiles = (len + tile - 1) / tile;
+  const int base = tiles / ns, extra = tiles % ns;
+  const int t0 = s * base + min(s, extra);
+  const int t1 = t0 + base + (s < extra ? 1 : 0);
+  kb0 = min(len, t0 * tile);
+  kb1 = min(len, t1 * tile);
+}
 // keys per split of a sequence of `len` keys cut into `nsplit_b` splits of whole tiles
 __host__ __device__ __forceinline__ int paged_chunk(int len, int nsplit_b, int tile_keys) {
   const int tiles = (len + tile_keys - 1) / tile_keys;
@@ -258,13 +272,14 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int hkv = blockIdx.y;
+  const int hkv = PAGED ? blockIdx.y : blockIdx.x;
   const int G = args.Hq / args.Hkv;
   // (sequence, split) of this CTA, this sequence's visible keys, split length and split count.
-  // Uniform batch: grid (split, kv head, batch).  Paged batch: grid (CTA, kv head); the CTAs of
+  // Uniform batch: grid (kv head, batch, split).  Paged batch: grid (CTA, kv head); the CTAs of
   // a kv head are shared out over the sequences in proportion to their lengths (in tiles), every
   // CTA computing the same plan from seq_lens; CTAs past the plan have nothing to do.
-  int b = blockIdx.z, split = blockIdx.x;
+  int b = PAGED ? 0 : static_cast<int>(blockIdx.y);
+  int split = PAGED ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.z);
   int sk_b = args.Sk_eff, chunk = args.chunk, nsplit_b = args.nsplit;
   int first = 0;  // paged: the plan index of this sequence's first CTA
   if constexpr (PAGED) {
@@ -296,8 +311,8 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
   const int64_t flag_base = PAGED ? static_cast<int64_t>(hkv) * args.nsplit + first
                                   : (static_cast<int64_t>(b) * args.Hkv + hkv) * args.nsplit;
   const int sk_lim = PAGED ? sk_b : args.Sk;  // keys stored (scale rows past it are not read)
-  const int kb0 = split * chunk;
-  const int kb1 = min(sk_b, kb0 + chunk);
+  int kb0 = split * chunk, kb1 = min(sk_b, kb0 + chunk);
+  if constexpr (!PAGED) uniform_split(split, nsplit_b, sk_b, kTileKeys, kb0, kb1);
   const int ntiles = (kb1 - kb0 + kTileKeys - 1) / kTileKeys;
   const int64_t bh = static_cast<int64_t>(b) * args.Hkv + hkv;
 
@@ -933,7 +948,8 @@ int decode_paged_ctas(int B, int Hkv, int num_sms, bool kq4, bool vq4) {
 
 void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool kq4, bool vq4, int* nsplit,
                  int* chunk) {
-  // one wave of CTAs at the kernel's resident count, equal key chunks of whole tiles
+  // one wave of CTAs at the kernel's resident count; the keys shared out in whole tiles as
+  // evenly as possible (uniform_split), chunk = the longer splits' length
   const int tile = decode_tile_keys(kq4, vq4);
   const int units = B * Hkv;
   const int slots = num_sms * decode_ctas_per_sm(kq4, vq4);
@@ -943,10 +959,8 @@ void decode_plan(int B, int Hkv, int Sk_eff, int num_sms, bool kq4, bool vq4, in
   if (ns > max_tiles) ns = max_tiles;
   if (ns > kMaxSplits) ns = kMaxSplits;
   if (ns < 1) ns = 1;
-  int ck = (Sk_eff + ns - 1) / ns;
-  ck = (ck + tile - 1) / tile * tile;
-  *chunk = ck;
-  *nsplit = (Sk_eff + ck - 1) / ck;
+  *chunk = (max_tiles + ns - 1) / ns * tile;
+  *nsplit = ns;
 }
 
 template <int D, bool BF16, bool KQ4, bool VQ4>
@@ -980,7 +994,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   a.chunk = L.chunk;
   a.scale_log2 = L.scale * kLog2e;
   // paged: nsplit CTAs per kv head shared over the batch (the plan is made on the device)
-  const dim3 grid = L.block_table ? dim3(L.nsplit, L.Hkv, 1) : dim3(L.nsplit, L.Hkv, L.B);
+  const dim3 grid = L.block_table ? dim3(L.nsplit, L.Hkv, 1) : dim3(L.Hkv, L.B, L.nsplit);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, a);
   return cudaGetLastError();
 }
@@ -1015,13 +1029,14 @@ int64_t decode_debug_schedule(const int32_t* seq_lens, int B, int Hkv, int Sk, i
     }
     ++n;
   };
-  if (seq_lens == nullptr) {  // uniform batch: grid (split, kv head, batch)
+  if (seq_lens == nullptr) {  // uniform batch: grid (kv head, batch, split)
     int ns = 1, ck = Sk;
     decode_plan(B, Hkv, Sk, num_sms, kq4, vq4, &ns, &ck);
     for (int b = 0; b < B; ++b)
       for (int sp = 0; sp < ns; ++sp) {
-        const int kb0 = sp * ck;
-        put(b, sp, ns, kb0, kb0 + ck < Sk ? kb0 + ck : Sk);
+        int kb0, kb1;
+        uniform_split(sp, ns, Sk, tile, kb0, kb1);
+        put(b, sp, ns, kb0, kb1);
       }
     return n;
   }

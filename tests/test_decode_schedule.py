@@ -1,9 +1,9 @@
 """The decode kernels' work split on the host (no device), read back through fa_decode_schedule
 and checked against the plan restated from its definition.
 
-Uniform batch (fa_fwd, Sq = 1): every (sequence, kv head) is cut into the same number of splits
-of whole tiles; the splits fill one wave of resident CTAs (3 per SM with q4_0 K and V, else 2),
-up to one split per tile.  Paged batch (fa_decode_paged): the CTAs of a kv head, one wave's
+Uniform batch (fa_fwd, Sq = 1): every (sequence, kv head) is cut into the same number of splits;
+the splits fill one wave of resident CTAs (3 per SM with q4_0 K and V, else 2), up to one split
+per tile, and share the key tiles out as evenly as whole tiles allow, the longer splits first.  Paged batch (fa_decode_paged): the CTAs of a kv head, one wave's
 worth (at least one per sequence), are shared out over the sequences: sequence b gets
 1 + floor((CTAs - B) * tiles_b / total tiles) consecutive CTAs, and its keys are cut into that
 many splits of ceil(tiles_b / splits) tiles.  Either way, every key of every sequence must
@@ -51,21 +51,28 @@ def test_uniform_split(fmt, B, Hkv, Sk, n):
         r = rows[rows[:, 0] == b]
         check_cover(r, Sk)
         assert (r[:, 4] > r[:, 3]).all()  # no empty split in a uniform batch
-        chunk = int(r[0, 4] - r[0, 3]) if ns > 1 else None
-        if chunk is not None:
-            assert chunk % tile == 0 and (r[:-1, 4] - r[:-1, 3] == chunk).all()
+        # whole tiles (the last split may end at Sk), lengths in tiles never growing, within one
+        tiles = -(-(r[:, 4] - r[:, 3]) // tile)
+        assert (r[:-1, 4] % tile == 0).all()
+        assert (np.diff(tiles) <= 0).all() and tiles.max() - tiles.min() <= 1
     assert ns == 1 or B * Hkv * ns <= n * ctas_per_sm(*fmt)  # one wave
-    want_ns, want_chunk = expected_uniform(B, Hkv, Sk, n, fmt)
-    assert ns == want_ns and (ns == 1 or chunk == want_chunk)
+    want = expected_uniform(B, Hkv, Sk, n, fmt)
+    assert [tuple(int(x) for x in row[3:5]) for row in rows[rows[:, 0] == 0]] == want
 
 
 def expected_uniform(B, Hkv, Sk, n, fmt):
-    """As many splits as one wave holds (at least 1, at most one per tile and 1024), then the
-    keys cut into equal chunks of whole tiles; the split count is what those chunks need."""
+    """As many splits as one wave holds (at least 1, at most one per tile and 1024); the key tiles
+    are shared out as evenly as whole tiles allow, the first (tiles mod splits) splits taking one
+    more.  Returns the (first key, end key) of each split."""
     tile = tile_keys(*fmt)
-    want = min(max(1, n * ctas_per_sm(*fmt) // (B * Hkv)), -(-Sk // tile), 1024)
-    chunk = -(-(-(-Sk // want)) // tile) * tile
-    return -(-Sk // chunk), chunk
+    tiles = -(-Sk // tile)
+    ns = min(max(1, n * ctas_per_sm(*fmt) // (B * Hkv)), tiles, 1024)
+    out, t = [], 0
+    for s in range(ns):
+        nt = tiles // ns + (1 if s < tiles % ns else 0)
+        out.append((min(Sk, t * tile), min(Sk, (t + nt) * tile)))
+        t += nt
+    return out
 
 
 def expected_paged(lens, cap, Hkv, n, fmt):
