@@ -337,8 +337,9 @@ int64_t fa_prefill_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q
  * decode sums (fa_fwd with Sq == 1, and fa_decode_paged): which CTA adds which keys, and the
  * splits that the launch merges.
  *  seq_lens == NULL: a uniform batch of B sequences of Sk keys each (fa_fwd decode at position
- *    Sk - 1): every (sequence, kv head) is cut into the same number of splits of whole tiles;
- *    one row per (sequence, split), B x splits rows.
+ *    Sk - 1): every (sequence, kv head) is cut into the same number of splits, the key tiles
+ *    shared out as evenly as whole tiles allow (the first tiles-mod-splits splits take one tile
+ *    more); one row per (sequence, split), B x splits rows.
  *  seq_lens != NULL (host array of B lengths): a paged batch (fa_decode_paged) whose pages hold
  *    page_size tokens, pages_per_seq per sequence; the CTAs of a kv head (the row count) are
  *    shared out over the sequences in proportion to their lengths, at least one each, every
