@@ -248,11 +248,6 @@ __host__ __device__ __forceinline__ void uniform_split(int s, int ns, int len, i
   kb0 = min(len, t0 * tile);
   kb1 = min(len, t1 * tile);
 }
-// keys per split of a sequence of `len` keys cut into `nsplit_b` splits of whole tiles
-__host__ __device__ __forceinline__ int paged_chunk(int len, int nsplit_b, int tile_keys) {
-  const int tiles = (len + tile_keys - 1) / tile_keys;
-  return (tiles + nsplit_b - 1) / nsplit_b * tile_keys;
-}
 
 template <int D, bool BF16, bool KQ4, bool VQ4, bool PAGED>
 __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>::kCtasPerSm)
@@ -272,21 +267,21 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int hkv = PAGED ? blockIdx.y : blockIdx.x;
+  const int hkv = blockIdx.x;
   const int G = args.Hq / args.Hkv;
   // (sequence, split) of this CTA, this sequence's visible keys, split length and split count.
-  // Uniform batch: grid (kv head, batch, split).  Paged batch: grid (CTA, kv head); the CTAs of
+  // Uniform batch: grid (kv head, batch, split).  Paged batch: grid (kv head, CTA); the CTAs of
   // a kv head are shared out over the sequences in proportion to their lengths (in tiles), every
   // CTA computing the same plan from seq_lens; CTAs past the plan have nothing to do.
   int b = PAGED ? 0 : static_cast<int>(blockIdx.y);
-  int split = PAGED ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.z);
-  int sk_b = args.Sk_eff, chunk = args.chunk, nsplit_b = args.nsplit;
+  int split = PAGED ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.z);
+  int sk_b = args.Sk_eff, nsplit_b = args.nsplit;
   int first = 0;  // paged: the plan index of this sequence's first CTA
   if constexpr (PAGED) {
     const int cap = args.pages_per_seq * args.page_size;
     PagedSlot ps;
     if (!paged_slot(args.seq_lens, args.B, cap, args.nsplit, kTileKeys,
-                    static_cast<int>(blockIdx.x), ps))
+                    static_cast<int>(blockIdx.y), ps))
       return;  // nothing planned for this CTA (no barrier or memory touched yet)
     b = ps.b;
     split = ps.split;
@@ -298,7 +293,6 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
         atomicCAS(&g_decode_error, kErrNone, kErrBadIndex);
       sk_b = max(1, min(sk_b, cap));
     }
-    chunk = paged_chunk(sk_b, nsplit_b, kTileKeys);
   }
   // slots of the partials and flags.  Uniform batch: [B, Hq, nsplit] partial rows, [B, Hkv,
   // nsplit] flags.  Paged batch: one slot per (kv head, plan CTA): [Hkv, nsplit, G] partial rows,
@@ -311,8 +305,8 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
   const int64_t flag_base = PAGED ? static_cast<int64_t>(hkv) * args.nsplit + first
                                   : (static_cast<int64_t>(b) * args.Hkv + hkv) * args.nsplit;
   const int sk_lim = PAGED ? sk_b : args.Sk;  // keys stored (scale rows past it are not read)
-  int kb0 = split * chunk, kb1 = min(sk_b, kb0 + chunk);
-  if constexpr (!PAGED) uniform_split(split, nsplit_b, sk_b, kTileKeys, kb0, kb1);
+  int kb0, kb1;
+  uniform_split(split, nsplit_b, sk_b, kTileKeys, kb0, kb1);
   const int ntiles = (kb1 - kb0 + kTileKeys - 1) / kTileKeys;
   const int64_t bh = static_cast<int64_t>(b) * args.Hkv + hkv;
 
@@ -994,7 +988,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, cudaStream_t stream) {
   a.chunk = L.chunk;
   a.scale_log2 = L.scale * kLog2e;
   // paged: nsplit CTAs per kv head shared over the batch (the plan is made on the device)
-  const dim3 grid = L.block_table ? dim3(L.nsplit, L.Hkv, 1) : dim3(L.Hkv, L.B, L.nsplit);
+  const dim3 grid = L.block_table ? dim3(L.Hkv, L.nsplit, 1) : dim3(L.Hkv, L.B, L.nsplit);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_k, L.tm_v, a);
   return cudaGetLastError();
 }
@@ -1048,9 +1042,9 @@ int64_t decode_debug_schedule(const int32_t* seq_lens, int B, int Hkv, int Sk, i
       continue;
     }
     const int len = paged_len(seq_lens, ps.b, cap);
-    const int ck = paged_chunk(len, ps.nsplit_b, tile);
-    const int kb0 = ps.split * ck;
-    put(ps.b, ps.split, ps.nsplit_b, kb0, kb0 + ck < len ? kb0 + ck : len);
+    int kb0, kb1;
+    uniform_split(ps.split, ps.nsplit_b, len, tile, kb0, kb1);
+    put(ps.b, ps.split, ps.nsplit_b, kb0, kb1);
   }
   return n;
 }

@@ -5,8 +5,9 @@ Uniform batch (fa_fwd, Sq = 1): every (sequence, kv head) is cut into the same n
 the splits fill one wave of resident CTAs (3 per SM with q4_0 K and V, else 2), up to one split
 per tile, and share the key tiles out as evenly as whole tiles allow, the longer splits first.  Paged batch (fa_decode_paged): the CTAs of a kv head, one wave's
 worth (at least one per sequence), are shared out over the sequences: sequence b gets
-1 + floor((CTAs - B) * tiles_b / total tiles) consecutive CTAs, and its keys are cut into that
-many splits of ceil(tiles_b / splits) tiles.  Either way, every key of every sequence must
+1 + floor((CTAs - B) * tiles_b / total tiles) consecutive CTAs, and its key tiles are shared out
+over that many splits as evenly as whole tiles allow (the longer splits first; a sequence with
+fewer tiles than splits leaves its last splits empty).  Either way, every key of every sequence must
 belong to exactly one split.
 """
 import numpy as np
@@ -60,19 +61,25 @@ def test_uniform_split(fmt, B, Hkv, Sk, n):
     assert [tuple(int(x) for x in row[3:5]) for row in rows[rows[:, 0] == 0]] == want
 
 
+def even_split(length, ns, tile):
+    """(first key, end key) of ns splits sharing the ceil(length / tile) tiles out as evenly as
+    whole tiles allow, the first (tiles mod ns) splits taking one more."""
+    tiles = -(-length // tile)
+    out, t = [], 0
+    for s in range(ns):
+        nt = tiles // ns + (1 if s < tiles % ns else 0)
+        out.append((min(length, t * tile), min(length, (t + nt) * tile)))
+        t += nt
+    return out
+
+
 def expected_uniform(B, Hkv, Sk, n, fmt):
     """As many splits as one wave holds (at least 1, at most one per tile and 1024); the key tiles
     are shared out as evenly as whole tiles allow, the first (tiles mod splits) splits taking one
     more.  Returns the (first key, end key) of each split."""
     tile = tile_keys(*fmt)
-    tiles = -(-Sk // tile)
-    ns = min(max(1, n * ctas_per_sm(*fmt) // (B * Hkv)), tiles, 1024)
-    out, t = [], 0
-    for s in range(ns):
-        nt = tiles // ns + (1 if s < tiles % ns else 0)
-        out.append((min(Sk, t * tile), min(Sk, (t + nt) * tile)))
-        t += nt
-    return out
+    ns = min(max(1, n * ctas_per_sm(*fmt) // (B * Hkv)), -(-Sk // tile), 1024)
+    return even_split(Sk, ns, tile)
 
 
 def expected_paged(lens, cap, Hkv, n, fmt):
@@ -108,8 +115,7 @@ def test_paged_split_random_mixes(fmt):
             r = rows[c:c + ns[b]]
             assert (r[:, 0] == b).all(), (trial, b)
             check_cover(r, L[b])
-            chunk = -(-(-(-L[b] // tile)) // ns[b]) * tile
-            assert (r[:, 3] == np.arange(ns[b]) * chunk).all()
+            assert [tuple(int(x) for x in row[3:5]) for row in r] == even_split(L[b], ns[b], tile)
             c += ns[b]
         assert c <= nt and (rows[c:, 0] == -1).all()
 
