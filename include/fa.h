@@ -344,7 +344,9 @@ int64_t fa_prefill_schedule(int B, int Hq, int Hkv, int Sq, int Sk, int D, int q
  *    page_size tokens, pages_per_seq per sequence; the CTAs of a kv head (the row count) are
  *    shared out over the sequences in proportion to their lengths, at least one each, every
  *    length clamped to [1, page_size * pages_per_seq] as the kernel does (which also reports
- *    the out-of-range length); one row per CTA.  Sk is ignored.
+ *    the out-of-range length), each sequence's key tiles shared out over its CTAs as evenly as
+ *    whole tiles allow (a sequence with fewer tiles than CTAs leaves the last ones empty); one
+ *    row per CTA.  Sk is ignored.
  * rows (max_rows x 5 int32, row-major, caller-owned; may be NULL when max_rows is 0):
  * {sequence (-1: the CTA has no work), split, splits of that sequence, first key, end key}.
  * Returns the number of rows (rows beyond max_rows are counted, not written), or -2 for
