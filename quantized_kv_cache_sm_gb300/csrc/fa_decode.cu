@@ -854,6 +854,31 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
     // (m_s, l_s) with the splits across the lanes, 32 at a time; the first 32 stay in registers
     float2 ml0 = make_float2(-INFINITY, 0.f);
     if (lane < nsplit_b) ml0 = __ldcg(reinterpret_cast<const float2*>(p + lane * ss));
+    // paged batch, up to kFast splits: their O rows are loaded in the same round trip as (m, l)
+    // (a merge sits at the end of the launch, where each round trip to L2 is exposed; measured
+    // -3 % on the paged workloads; the uniform kernel keeps the loop below, where the extra
+    // registers cost more than they gain)
+    constexpr int kFast = PAGED ? 16 : 1;
+    const bool fast = PAGED && nsplit_b <= kFast;
+    float xf[kFast][kPer];
+    if (fast) {
+#pragma unroll
+      for (int j = 0; j < kFast; ++j) {
+        const float* row = p + j * ss + 4;
+        if (j < nsplit_b) {
+          if constexpr (kPer == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(row) + lane);
+            xf[j][0] = v.x; xf[j][1] = v.y; xf[j][2] = v.z; xf[j][3] = v.w;
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(row) + lane);
+            xf[j][0] = v.x; xf[j][1] = v.y;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) xf[j][e] = 0.f;
+        }
+      }
+    }
     float M = ml0.x;
     for (int s = lane + 32; s < nsplit_b; s += 32) M = fmaxf(M, __ldcg(p + s * ss));
 #pragma unroll
@@ -862,7 +887,17 @@ __global__ void __launch_bounds__(DCfg<D, KQ4, VQ4>::kThreads, DCfg<D, KQ4, VQ4>
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    for (int s0 = 0; s0 < nsplit_b; s0 += 32) {
+    if (fast) {
+      const float wl = (ml0.x == -INFINITY) ? 0.f : ex2(ml0.x - M);  // e^(m_s - M), lane s
+      L = wl * ml0.y;
+#pragma unroll
+      for (int j = 0; j < kFast; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, wl, j);
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[e] = fmaf(wj, xf[j][e], acc[e]);
+      }
+    }
+    for (int s0 = 0; s0 < (fast ? 0 : nsplit_b); s0 += 32) {
       float2 ml = ml0;
       if (s0 > 0) {
         ml = make_float2(-INFINITY, 0.f);
