@@ -314,7 +314,10 @@ fa_status fa_debug_wait_timeout(int64_t limit_ns, fa_stream_t stream);
  * 128-key blocks holding any key visible to tile A or B.  Units are ordered by pair index from
  * the last query tiles to the first, then batch, then head, and their steps concatenated into W
  * steps.  When the plan cuts (D = 128, more units than SMs, and an estimate favours it), CTA c
- * of num_sms runs the steps [floor(c W / num_sms), floor((c + 1) W / num_sms)).
+ * of num_sms runs the steps [floor(c W / num_sms), floor((c + 1) W / num_sms)).  When it keeps
+ * one unit per CTA and twice the units fit on the SMs at once (2 x units <= num_sms, more than
+ * one query tile), that launch gives each query tile a CTA of its own instead of a pair (tile B
+ * absent), so that no two tiles share an SM; the result is the same.
  *
  * plan (5 values, may be NULL): {cut (1) or one unit per CTA (0), CTAs of the cut launch (0 when
  * not cut), W, units, workspace bytes the cut needs}.  force_cut != 0 lays the cuts out over

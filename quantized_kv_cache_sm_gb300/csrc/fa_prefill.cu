@@ -134,6 +134,9 @@ struct PrefillArgs {
   float* p_max;            // optional [B, Hq, Sq]: a bound on the largest P the row's softmax
                            // wrote (see softmax_block)
   int B, Hq, Hkv, Sq, Sk, q_pos_offset, causal, n_qtiles, n_pairs;
+  // prefill_kernel: query rows per work unit, 256 (a pair of consecutive tiles) or 128 (one
+  // tile per CTA, tile B absent; n_pairs then counts query tiles)
+  int unit_rows;
   int Scap;  // tokens per (batch, kv head) in the K/V tensors (row stride); Sk <= Scap
   float scale_log2;
   // cut schedule (prefill_seg_kernel): W key-block steps in all, CTA c runs steps
@@ -559,17 +562,18 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // work unit: a pair of consecutive query tiles of one head, longest pairs first (the slowest
-  // grid dimension enumerates pairs); tile B may lie past Sq (odd tile count)
+  // grid dimension enumerates units); tile B may lie past Sq (odd tile count).  With
+  // unit_rows = 128 each unit is one query tile and tile B is absent.
   const int h = blockIdx.x;
   const int b = blockIdx.y;
-  const int pair = args.n_pairs - 1 - static_cast<int>(blockIdx.z);
-  const int q0A = 2 * pair * kBM;
+  const int unit = args.n_pairs - 1 - static_cast<int>(blockIdx.z);
+  const int q0A = unit * args.unit_rows;
   const int q0B = q0A + kBM;
   const int g = h / (args.Hq / args.Hkv);
   const int nbA = tile_blocks(args, q0A);
-  const int nbB = tile_blocks(args, q0B);
+  const int nbB = args.unit_rows == kBM ? 0 : tile_blocks(args, q0B);
   const int nbmax = max(nbA, nbB);  // causal rows further down see at least as many keys
-  const bool hasB = q0B < args.Sq;
+  const bool hasB = nbB > 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
@@ -1942,7 +1946,14 @@ static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   a.q_pos_offset = L.q_pos_offset;
   a.causal = L.causal;
   a.n_qtiles = (L.Sq + kBM - 1) / kBM;
-  a.n_pairs = (a.n_qtiles + 1) / 2;
+  // one query tile per CTA when even that many CTAs fit on the SMs at once: the two tiles of a
+  // pair share the SM sub-partitions for their softmax, so a lone tile steps faster, and
+  // with idle SMs the pair's longer chain is what the launch waits for
+  const int pairs = (a.n_qtiles + 1) / 2;
+  const bool single = a.n_qtiles > 1 && L.num_sms > 0 &&
+                      2LL * L.B * L.Hq * pairs <= static_cast<int64_t>(L.num_sms);
+  a.n_pairs = single ? a.n_qtiles : pairs;
+  a.unit_rows = single ? kBM : 2 * kBM;
   a.scale_log2 = L.scale * kLog2e;
   a.W = 0;  // one unit per CTA from the grid coordinates; the cut-schedule fields are unused
   a.n_ctas = 0;

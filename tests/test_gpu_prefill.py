@@ -67,6 +67,20 @@ def test_prefill_small_full_compare(fa, case):
     run_case(fa, *case, seed=7)
 
 
+@pytest.mark.parametrize("kv", ["dense", "q4_0"])
+@pytest.mark.parametrize("mapping", ["one_tile_per_cta", "tile_pairs"])
+def test_unit_mapping_on_either_side_of_the_threshold(fa, mapping, kv):
+    """One unit per CTA gives each 128-row query tile a CTA of its own when twice the pair units
+    fit on the SMs at once (2 x units <= SMs), else a pair of tiles per CTA.  A shape on each
+    side of that threshold for this device's SM count, every element against the oracle; three
+    ragged query tiles, so the last pair has no tile B either way."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs = 2  # per head: tiles (0, 1) and (2, -)
+    Hq = max(1, sms // (2 * pairs)) if mapping == "one_tile_per_cta" else sms // (2 * pairs) + 1
+    assert (2 * Hq * pairs <= sms) == (mapping == "one_tile_per_cta")
+    run_case(fa, 1, Hq, 1, 3 * 128 - 37, 600, 128, True, 600 - (3 * 128 - 37), "f16", kv, seed=5)
+
+
 def test_selfattn_b2_s512_h8_d64_full(fa):
     w = fa_inputs.WORKLOADS["selfattn_b2_s512_h8_d64_f16"]
     err, _ = run_case(fa, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True, 0, w.dtype, "dense", w.seed)
