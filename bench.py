@@ -11,6 +11,9 @@ prefill, the 2K/8K and bf16 prefill shapes and the q4_0 cache build.
 
 Timing: CUDA events on the launching stream around each launch; the L2 cache is flushed (a
 256 MiB write) before every timed prefill launch; decode reads 302 MB per call, more than L2.
+The legs of 2048 keys or fewer also report ``graph_us``: the device time per call of 20 calls
+replayed from one CUDA graph (no launch cost between calls, no L2 flush), beside their
+per-launch event time, which for calls this short includes microseconds of launch overhead.
 Multi-GPU: one process per GPU (torchrun); every rank runs a replica of the workload (independent
 problems, weak scaling); barrier + synchronize around the timed region, time = max over ranks.
 
@@ -435,6 +438,32 @@ def decode_leg(fa, dev, stream, peaks, peaks_src):
     }
 
 
+def graph_time_us(make_call, calls: int = 20, replays: int = 30) -> float:
+    """Device time per call (us) of `calls` back-to-back calls replayed from one CUDA graph, as
+    a serving loop runs short calls: no host launch cost between them and no L2 flush (a short
+    call's inputs stay in L2).  make_call(stream) returns the call bound to that stream."""
+    gs = torch.cuda.Stream()
+    call = make_call(gs)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(gs):
+        for _ in range(3):
+            call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        for _ in range(calls):
+            call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(gs):
+        g.replay()
+        e0.record(gs)
+        for _ in range(replays):
+            g.replay()
+        e1.record(gs)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (calls * replays)
+
+
 def other_legs(fa, dev, stream, flush, peaks):
     out = {}
     peak = peaks["bf16_tflops"]
@@ -451,13 +480,17 @@ def other_legs(fa, dev, stream, flush, peaks):
         n = fa.fa_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.q_pos_offset, w.causal)
         ws = torch.empty(n, dtype=torch.uint8, device=dev) if n > 0 else None
 
-        def call():
-            fa.fa_fwd_ex(q, k, v, o, causal=True, q_pos_offset=w.q_pos_offset, scale=w.scale,
-                         workspace=ws, stream=stream)
+        def bound(st):
+            return lambda: fa.fa_fwd_ex(q, k, v, o, causal=True, q_pos_offset=w.q_pos_offset,
+                                        scale=w.scale, workspace=ws, stream=st)
 
-        ms = time_calls(call, 50, 5, flush=flush, stream=stream)
+        ms = time_calls(bound(stream), 50, 5, flush=flush, stream=stream)
         tf = w.flops() / (ms * 1e-3) / 1e12
         out[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 2), "frac": round(tf / peak, 4)}
+        if w.Sk <= 2048:
+            # a call this short is paced by its launch as much as by the kernel: also its time
+            # per call replayed from a CUDA graph (warm L2, no launch cost between calls)
+            out[name]["graph_us"] = round(graph_time_us(bound), 2)
     # f16 K with a q4_0 V (independent cache formats): 16K chunked prefill and 64K decode
     w = fa_inputs.WORKLOADS["prefill_gqa32x8_d128_sq2048_sk16384_f16"]
     q, k, v = fa_inputs.make_qkv(w, device=dev, generate_on_device=True)
