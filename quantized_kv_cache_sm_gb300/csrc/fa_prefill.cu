@@ -407,11 +407,18 @@ __device__ __forceinline__ bool block_row_p_chunked(uint32_t scol, int rel_lim, 
 // frame in force for its block: the exact largest P of a block that ran the frame test (P is
 // monotonic in the score), the block's sum of P otherwise (at least its largest P, and below
 // kSumTrigger).  Either way pmx <= e^10 whenever the frame rule holds.
-template <int D, bool BF16, bool ONE_READ, bool CHUNKED = false>
+struct NoWait {
+  __device__ void operator()() const {}
+};
+// wait_o runs before O is rescaled in tensor memory (a PV MMA may still be adding to it when the
+// S buffers alternate within one query tile)
+template <int D, bool BF16, bool ONE_READ, bool CHUNKED = false, class WaitO = NoWait>
 __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool need_mask,
                                               int rel_lim, float sl2, bool o_live, float& f,
-                                              float& l, int& nres, float& pmx) {
+                                              float& l, int& nres, float& pmx,
+                                              const WaitO& wait_o = WaitO()) {
   auto rescale_o = [&](float alpha) {
+    wait_o();
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t r[32];
@@ -544,7 +551,8 @@ __host__ __device__ __forceinline__ int tile_blocks(const PrefillArgs& a, int q0
   return (kend + kBN - 1) / kBN;
 }
 
-template <int D, bool BF16, bool KQ4, bool VQ4>
+// ALT: one query tile per CTA (dense K/V) whose key blocks alternate between the two S buffers
+template <int D, bool BF16, bool KQ4, bool VQ4, bool ALT>
 __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
@@ -746,16 +754,17 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
         return s;
       };
       auto release = [&](int s) { mma_commit(bar(kBarRingEmpty + s)); };
-      auto issue_qk = [&](int t, int s) {
+      // QK of query tile t into S buffer sb (tile t's own, except in the alternating mode)
+      auto issue_qk = [&](int t, int s, int sb) {
         const uint32_t qaddr = sbase + C::kOffQ + t * C::kQBytes;
         const uint32_t kaddr = sbase + C::kOffRing + s * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          mma_ss(tmem + col_s(t), make_sdesc_sw128(qaddr + off, 16, 1024),
+          mma_ss(tmem + col_s(sb), make_sdesc_sw128(qaddr + off, 16, 1024),
                  make_sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(kBarSFull + t));
+        mma_commit(bar(kBarSFull + sb));
       };
       auto issue_pv = [&](int t, int j, int s, int nb_t) {
         ok = ok && mbar_wait(bar(kBarPReady + t), j & 1, abort_flag, &g_prefill_error);
@@ -769,6 +778,23 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
                  make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
                  (j > 0 || kk > 0) ? 1u : 0u);
         if (j == nb_t - 1) mma_commit(bar(kBarODone + t));
+      };
+      // PV of block j of a lone query tile whose blocks alternate between the S buffers; tile
+      // B's O-done barrier, unused then, completes after every PV (the softmax waits for it
+      // before it rescales O)
+      auto issue_pv_alt = [&](int j, int s, int nb_t) {
+        const int sb = j & 1;
+        ok = ok && mbar_wait(bar(kBarPReady + sb), (j >> 1) & 1, abort_flag, &g_prefill_error);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + C::kColO0, tmem + col_s(sb) + kk * 8,
+                 make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(kBarODone + 1));
+        if (j == nb_t - 1) mma_commit(bar(kBarODone));
       };
       // order: QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage is
       // acquired at the start of the step that first uses it and released after its last use
@@ -784,12 +810,37 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
           ++gn;
           return p;
         };
+        if constexpr (ALT) {
+          // one query tile whose key blocks alternate between the two S buffers: QK(j + 2) goes
+          // into block j's buffer right after PV(j) has read P from it, so the softmax finds
+          // block j + 1's scores ready when it finishes block j.  Slot 0 holds K(0), slot g
+          // holds V(g - 1) and K(g).
+          int pvs = 0;  // the slot holding the V of the next PV
+          if (nbA > 0 && ok) {
+            const int p = acquire_g();
+            if (ok) {
+              issue_qk(0, 2 * p, 0);
+              release(p);
+              pvs = acquire_g();
+              if (ok && nbA > 1) issue_qk(0, 2 * pvs, 1);
+            }
+          }
+          for (int j = 0; j < nbA && ok; ++j) {
+            issue_pv_alt(j, 2 * pvs + 1, nbA);
+            if (!ok) break;
+            release(pvs);
+            if (j + 1 < nbA) {
+              pvs = acquire_g();
+              if (ok && j + 2 < nbA) issue_qk(0, 2 * pvs, j & 1);
+            }
+          }
+        } else {
         if (nbmax > 0 && ok) {
           const int p = acquire_g();
           if (ok) {
-            if (nbA > 0) issue_qk(0, 2 * p);
+            if (nbA > 0) issue_qk(0, 2 * p, 0);
             if (nbB > 0)
-              issue_qk(1, 2 * p);  // tile B's softmax releases the slot
+              issue_qk(1, 2 * p, 1);  // tile B's softmax releases the slot
             else
               release(p);
           }
@@ -800,20 +851,21 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
           if (!ok) break;
           if (j < nbA) issue_pv(0, j, 2 * p + 1, nbA);
           if (!ok) break;
-          if (next && j + 1 < nbA) issue_qk(0, 2 * p);
+          if (next && j + 1 < nbA) issue_qk(0, 2 * p, 0);
           if (j < nbB) issue_pv(1, j, 2 * p + 1, nbB);
           if (!ok) break;
           if (next && j + 1 < nbB)
-            issue_qk(1, 2 * p);
+            issue_qk(1, 2 * p, 1);
           else
             release(p);
+        }
         }
       } else {
       if (nbmax > 0 && ok) {
         const int sK = acquire();
         if (ok) {
-          if (nbA > 0) issue_qk(0, sK);
-          if (nbB > 0) issue_qk(1, sK);
+          if (nbA > 0) issue_qk(0, sK, 0);
+          if (nbB > 0) issue_qk(1, sK, 1);
           release(sK);
         }
       }
@@ -827,12 +879,12 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
         if (!ok) break;
         if (j < nbA) issue_pv(0, j, sV, nbA);
         if (!ok) break;
-        if (next && j + 1 < nbA) issue_qk(0, sK);
+        if (next && j + 1 < nbA) issue_qk(0, sK, 0);
         if (j < nbB) issue_pv(1, j, sV, nbB);
         if (!ok) break;
         release(sV);
         if (next) {
-          if (j + 1 < nbB) issue_qk(1, sK);
+          if (j + 1 < nbB) issue_qk(1, sK, 1);
           release(sK);
         }
       }
@@ -853,16 +905,22 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
     const int qrow = q0 + row;
     const int pos = args.q_pos_offset + qrow;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t scol = tmem + lane_off + col_s(t);
+    const uint32_t scol_t = tmem + lane_off + col_s(t);
     const uint32_t ocol = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
     const float sl2 = args.scale_log2;
+    // a lone query tile (dense K/V) alternates its key blocks between the two S buffers
+    constexpr bool alt = ALT;
+    static_assert(!ALT || C::kPaired, "alternating S buffers need the paired dense ring");
     float f = -INFINITY;  // frame, base-2 units of the scaled score
     float l = 0.f;
     int nres = 0;
     float pmx = -INFINITY;  // bound on the largest P written
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
-      ok = mbar_wait(bar(kBarSFull + t), j & 1, abort_flag, &g_prefill_error);
+      const int sb = alt ? (j & 1) : t;  // S buffer of this block
+      const uint32_t scol = alt ? tmem + lane_off + col_s(sb) : scol_t;
+      ok = mbar_wait(bar(kBarSFull + sb), alt ? ((j >> 1) & 1) : (j & 1), abort_flag,
+                     &g_prefill_error);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -877,11 +935,22 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
           (kb + kBN > args.Sk) || (args.causal && kb + kBN - 1 > args.q_pos_offset + q0);
       // last visible key of this row, relative to the block
       const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
-      softmax_block<D, BF16, !C::kWide, C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > 0, f,
-                                                  l, nres, pmx);
+      if constexpr (alt) {
+        // PV(j - 1) may still be adding to O when this block moves the frame; PV(j) cannot
+        // have started, so the PV-done barrier has completed j - 1 or j times
+        auto wait_pv = [&]() {
+          mbar_wait(bar(kBarODone + 1), (j - 1) & 1, abort_flag, &g_prefill_error);
+          tc_fence_after();
+        };
+        softmax_block<D, BF16, !C::kWide, C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > 0,
+                                                    f, l, nres, pmx, wait_pv);
+      } else {
+        softmax_block<D, BF16, !C::kWide, C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > 0,
+                                                    f, l, nres, pmx);
+      }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kBarPReady + t));
+      mbar_arrive(bar(kBarPReady + sb));
     }
     if (ok && nb > 0) {
       // the tile's last PV MMA completing implies all of its MMAs have
@@ -1927,10 +1996,6 @@ template <int D, bool BF16, bool KQ4, bool VQ4>
 static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   using C = Cfg<D, KQ4, VQ4, true>;
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory budget");
-  auto kern = prefill_kernel<D, BF16, KQ4, VQ4>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
-  if (e != cudaSuccess) return e;
   PrefillArgs a{};
   a.o = L.o;
   a.k_scale = static_cast<const uint8_t*>(L.k_scale);
@@ -1960,6 +2025,14 @@ static cudaError_t launch_t(const PrefillLaunch& L, cudaStream_t stream) {
   a.part = nullptr;
   a.pflags = nullptr;
   a.tag = 0;
+  // a lone query tile with dense K/V also alternates its key blocks between the two S buffers;
+  // that form is its own instantiation, so the pair form's code is untouched by it
+  constexpr bool kAlt = !KQ4 && !VQ4;
+  auto kern = (single && kAlt) ? prefill_kernel<D, BF16, KQ4, VQ4, kAlt>
+                               : prefill_kernel<D, BF16, KQ4, VQ4, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
   dim3 grid(L.Hq, L.B, a.n_pairs);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(L.tm_q, L.tm_k, L.tm_v, a);
   return cudaGetLastError();
