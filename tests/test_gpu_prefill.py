@@ -81,6 +81,23 @@ def test_unit_mapping_on_either_side_of_the_threshold(fa, mapping, kv):
     run_case(fa, 1, Hq, 1, 3 * 128 - 37, 600, 128, True, 600 - (3 * 128 - 37), "f16", kv, seed=5)
 
 
+@pytest.mark.parametrize("D,dtype", [(128, "f16"), (64, "bf16")])
+def test_score_ramp_on_lone_query_tiles(fa, D, dtype):
+    """Frame moves in the one-tile-per-CTA launch, where a dense tile's key blocks alternate
+    between the two S buffers and each O rescale must wait for the previous block's PV.  The
+    2.0-per-block score ramp moves every row's frame about every fifth block; every element is
+    checked against the oracle and every row must have moved its frame more than once."""
+    B, Hq, Hkv, Sq, Sk = 1, 8, 2, 256, 4096
+    assert 2 * B * Hq <= torch.cuda.get_device_properties(0).multi_processor_count
+    _, counts = run_case(fa, B, Hq, Hkv, Sq, Sk, D, True, Sk - Sq, dtype, "dense", seed=3,
+                         ramp=True, counts=True)
+    per_row = counts.reshape(-1, Sq)
+    assert (per_row >= 2).all(), "the deferred rescale branch never ran on some row"
+    nblocks = (Sk - Sq + np.arange(Sq)) // 128 + 1
+    ratio = per_row / (1 + (nblocks - 1) / 5.0)[None, :]
+    assert 0.7 < ratio.mean() < 1.3, ratio.mean()
+
+
 def test_selfattn_b2_s512_h8_d64_full(fa):
     w = fa_inputs.WORKLOADS["selfattn_b2_s512_h8_d64_f16"]
     err, _ = run_case(fa, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True, 0, w.dtype, "dense", w.seed)
