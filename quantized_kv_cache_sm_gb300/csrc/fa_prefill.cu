@@ -17,7 +17,10 @@
 //    tiles;
 //  * S = Q K^T and O += P V are tcgen05.mma into tensor memory; the single MMA thread
 //    interleaves the tiles (PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1)) so the tensor core works on
-//    one tile while the softmax warps of the other run;
+//    one tile while the softmax warps of the other run.  When even one query tile per CTA
+//    leaves SMs idle (2 x pair units <= SMs), each CTA takes one tile instead, and with dense
+//    K/V that tile's key blocks alternate between the two S buffers (QK(j+2) is issued right
+//    after PV(j)), so the softmax finds the next block's scores ready;
 //  * the softmax warps own one row each: block max, the deferred rescale, P = 2^(t - f) written
 //    back over S as f16/bf16 for the PV MMA, running row sum l;
 //  * deferred rescale ("perf(rocm): defer SDPA accumulator rescale, stage Q once per block
@@ -25,12 +28,13 @@
 //    more than 10 natural-log units; only then are O and l multiplied by e^(f_old - f_new).
 //    P stays below e^10 = 22026 in every frame.
 //
-// Warp roles (12 warps):
-//   warp 0       TMA producer (one lane)
-//   warp 1       TMEM allocator + MMA issuer (one lane)
-//   warps 2, 3   q4_0 dequant (q4_0 variant only; idle otherwise), two key rows per thread
-//   warps 4..7   softmax / rescale / epilogue of query tile A, one row per thread
-//   warps 8..11  the same for query tile B
+// Warp roles (12 warps with dense K/V, 16 with a q4_0 side):
+//   warp 0        TMA producer (one lane)
+//   warp 1        TMEM allocator + MMA issuer (one lane)
+//   warps 2, 3    q4_0 dequant with warps 12..15 (six warps sharing each raw tile's items);
+//                 idle with dense K/V
+//   warps 4..7    softmax / rescale / epilogue of query tile A, one row per thread
+//   warps 8..11   the same for query tile B
 #include <algorithm>
 
 #include "fa_internal.h"
