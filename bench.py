@@ -353,7 +353,7 @@ def e2e_leg(fa, w, dev, stream, steps, warmup, world):
     - the reported value: consecutive steps alternate between two streams with their own device
       buffers, so step i+1's host-to-device copies run while step i computes and step i's
       read-back overlaps step i+1 -- the steady state of a serving loop; every step still moves
-      all of its own bytes, and the host link (one direction at a time) is shared by both."""
+      all of its own bytes over the one host link, whose two directions share its bandwidth."""
     q, k, v = fa_inputs.make_qkv(w, device=dev, generate_on_device=True)
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
