@@ -113,14 +113,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Programmatic dependent launch: let the next kernel in the stream start its prologue early
-// (issued by every CTA of the primary grid), and wait in the secondary for the primary's results.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_primary() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
 
 // ------------------------------------------------------------------------------------------
 // TMA and cp.async
