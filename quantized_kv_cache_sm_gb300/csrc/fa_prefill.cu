@@ -88,10 +88,11 @@ struct Cfg {
   static constexpr int kBarBytes = 512 + 1024;  // barriers, flags, then the segment table
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   // warps: 0 producer, 1 MMA issuer, 4-11 softmax (one thread per query row), 2-3 dequant
-  // with q4_0 K or V; WIDE adds dequant warps 12-15 (sixteen warps, so 128 registers a thread:
-  // the softmax then reads S in 32-key chunks).  Measured at 16K keys, q4_0 K and V: with two
-  // dequant warps the step waits for dequantized tiles; six of them and the chunked read take
-  // the cut kernel from 0.477 to 0.410 ms and the one-unit kernel from 0.484 to 0.443 ms.
+  // with q4_0 K or V; WIDE adds dequant warps 12-15 (sixteen warps, 128 registers a thread at
+  // launch; the kernels then move registers from warpgroups 0 and 3 to the two softmax
+  // warpgroups, 88 and 168 a thread).  Measured at 16K keys, q4_0 K and V: with two dequant
+  // warps the step waits for dequantized tiles; six of them took the cut kernel from 0.477 to
+  // 0.410 ms and the one-unit kernel from 0.484 to 0.443 ms.
   static constexpr bool kWide = WIDE && kAnyQ4;
   static constexpr int kDqWarps = kAnyQ4 ? (kWide ? 6 : 2) : 0;
   static constexpr int kDqThreads = kDqWarps * 32;
@@ -212,71 +213,6 @@ struct Dq<true> {
   }
 };
 
-// Softmax over one 128-key block of one row (this thread's TMEM lane, columns scol..scol+127).
-// MASK: hide the keys with index > rel_lim (relative to the block); only blocks straddling the
-// diagonal or the key tail need it, the others use the branch-free instantiation.
-template <bool MASK>
-__device__ __forceinline__ float block_row_max(uint32_t scol, int rel_lim) {
-  float mx = -INFINITY;
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    uint32_t r0[32], r1[32];
-    tmem_ld32(scol + 64 * hf, r0);
-    tmem_ld32(scol + 64 * hf + 32, r1);
-    tmem_wait_ld();
-    reg_fence32(r0);
-    reg_fence32(r1);
-    float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      float a0 = __uint_as_float(r0[i]), a1 = __uint_as_float(r0[i + 1]);
-      float c0 = __uint_as_float(r1[i]), c1 = __uint_as_float(r1[i + 1]);
-      if (MASK) {
-        if (64 * hf + i > rel_lim) a0 = -INFINITY;
-        if (64 * hf + i + 1 > rel_lim) a1 = -INFINITY;
-        if (64 * hf + 32 + i > rel_lim) c0 = -INFINITY;
-        if (64 * hf + 33 + i > rel_lim) c1 = -INFINITY;
-      }
-      m0 = fmax3(m0, a0, a1);
-      m1 = fmax3(m1, c0, c1);
-    }
-    mx = fmax3(mx, m0, m1);
-  }
-  return mx;
-}
-// P = 2^(s * sl2 + nf) for the block, packed in pairs over the first half of the S columns
-// (keys 32 c .. 32 c + 31 -> packed columns 16 c .. 16 c + 15, whose S values are already read);
-// returns the row sum of P.
-template <bool MASK, bool BF16>
-__device__ __forceinline__ float block_row_exp(uint32_t scol, int rel_lim, float sl2, float nf) {
-  // the scale-and-shift and the row sum run two keys per instruction (packed f32 pairs)
-  const uint64_t sl2x2 = f2_pack(sl2, sl2), nfx2 = f2_pack(nf, nf);
-  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-  for (int c = 0; c < kBN / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(scol + 32 * c, r);
-    tmem_wait_ld();
-    reg_fence32(r);
-    uint32_t pr[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
-      if (MASK) {
-        if (32 * c + 2 * i > rel_lim) s0 = -INFINITY;
-        if (32 * c + 2 * i + 1 > rel_lim) s1 = -INFINITY;
-      }
-      const float2 t = f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, nfx2));
-      const float p0 = ex2(t.x), p1 = ex2(t.y);
-      const uint64_t pp = f2_pack(p0, p1);
-      if (i & 1) acc1 = f2_add(acc1, pp); else acc0 = f2_add(acc0, pp);
-      pr[i] = pack2<BF16>(p0, p1);
-    }
-    tmem_st16(scol + 16 * c, pr);
-  }
-  const float2 a = f2_unpack(f2_add(acc0, acc1));
-  return a.x + a.y;
-}
 
 template <bool BF16>
 __device__ __forceinline__ float block_row_exp_regs(uint32_t scol, const float (&s)[kBN],
@@ -351,49 +287,6 @@ __device__ __forceinline__ float row_max_regs(const float (&s)[kBN]) {
 // of the exponential cannot hide a P at the bound.
 constexpr float kSumTrigger = 21800.f;
 
-// Single read of S(j) in 32-key chunks (one TMEM wait each) for kernels with 128 registers a
-// thread: P = 2^(s * sl2 + nf) in the current frame, kept packed in registers (64 of them) until
-// the warp knows that no row's sum exceeds kSumTrigger; then P is stored over S's first half,
-// its row sum goes to sum and the result is true.  Otherwise nothing is stored (S(j) is intact)
-// and the result is false.
-template <bool MASK, bool BF16>
-__device__ __forceinline__ bool block_row_p_chunked(uint32_t scol, int rel_lim, float sl2,
-                                                    float nf, float& sum) {
-  const uint64_t sl2x2 = f2_pack(sl2, sl2), nfx2 = f2_pack(nf, nf);
-  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-  uint32_t pr[kBN / 2];
-#pragma unroll
-  for (int c = 0; c < kBN / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(scol + 32 * c, r);
-    tmem_wait_ld();
-    reg_fence32(r);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
-      if (MASK) {
-        if (32 * c + 2 * i > rel_lim) s0 = -INFINITY;
-        if (32 * c + 2 * i + 1 > rel_lim) s1 = -INFINITY;
-      }
-      const float2 t = f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, nfx2));
-      const float p0 = ex2(t.x), p1 = ex2(t.y);
-      const uint64_t pp = f2_pack(p0, p1);
-      if (i & 1) acc1 = f2_add(acc1, pp); else acc0 = f2_add(acc0, pp);
-      pr[16 * c + i] = pack2<BF16>(p0, p1);
-    }
-  }
-  const float2 a = f2_unpack(f2_add(acc0, acc1));
-  sum = a.x + a.y;
-  if (__any_sync(0xffffffffu, sum > kSumTrigger)) return false;
-#pragma unroll
-  for (int c = 0; c < kBN / 32; ++c) {
-    uint32_t q[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = pr[16 * c + i];
-    tmem_st16(scol + 16 * c, q);
-  }
-  return true;
-}
 
 // One key block of the online softmax for this thread's query row: read S(j), move the frame f
 // to the block max when that exceeds f by more than the margin (l and, when it already holds
@@ -401,11 +294,9 @@ __device__ __forceinline__ bool block_row_p_chunked(uint32_t scol, int rel_lim, 
 // its row sum to l.  O may be rescaled in place: S(j) being ready means PV(j-1) has completed
 // (QK(j) was issued after it).  The caller waits for the TMEM stores.
 //
-// ONE_READ selects the single-read form (one TMEM wait per block, 128 scores in registers,
-// P formed in the current frame first) over the two-pass form (the row max from tensor memory,
-// then P: six waits, fewer live registers).  Measured per kernel: the single read is faster in
-// the one-unit-per-CTA kernel and in the cut-schedule kernel with at least one dense side, the
-// two passes in the cut-schedule kernel with q4_0 K and V.
+// One TMEM wait per block: the 128 scores stay in registers (168 a thread in every layout;
+// with q4_0 sides by a register split between warpgroups) and P is formed in the current frame
+// first.
 //
 // pmx tracks a bound on the largest P written (before its rounding to the dtype), each in the
 // frame in force for its block: the exact largest P of a block that ran the frame test (P is
@@ -416,7 +307,7 @@ struct NoWait {
 };
 // wait_o runs before O is rescaled in tensor memory (a PV MMA may still be adding to it when the
 // S buffers alternate within one query tile)
-template <int D, bool BF16, bool ONE_READ, bool CHUNKED = false, class WaitO = NoWait>
+template <int D, bool BF16, class WaitO = NoWait>
 __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool need_mask,
                                               int rel_lim, float sl2, bool o_live, float& f,
                                               float& l, int& nres, float& pmx,
@@ -448,60 +339,31 @@ __device__ __forceinline__ void softmax_block(uint32_t scol, uint32_t ocol, bool
     }
     return __any_sync(0xffffffffu, need);
   };
-  if constexpr (ONE_READ) {
-    const bool first = __any_sync(0xffffffffu, f == -INFINITY);
-    float s[kBN];
-    if (need_mask)
-      block_row_scores<true>(scol, rel_lim, s);
-    else
-      block_row_scores<false>(scol, rel_lim, s);
-    float sum = 0.f;
-    bool done = false;
-    if (!first) {
-      sum = block_row_exp_regs<BF16>(scol, s, sl2, -f);
-      done = !__any_sync(0xffffffffu, sum > kSumTrigger);
-    }
-    if (done) {
-      pmx = fmaxf(pmx, sum);
-    } else {
-      const float mx = row_max_regs(s);
-      float alpha;
-      const bool any = frame_test(mx, alpha);
-      if (any || first) {
-        sum = block_row_exp_regs<BF16>(scol, s, sl2, -f);
-        if (any && o_live) rescale_o(alpha);
-      }
-      pmx = fmaxf(pmx, ex2(fmaf(mx, sl2, -f)));  // -inf keys (a masked row) give 0
-    }
-    l += sum;
-  } else {
-    if constexpr (CHUNKED) {
-      // the chunked single read first (not on a row's first block, whose frame is unset)
-      if (!__any_sync(0xffffffffu, f == -INFINITY)) {
-        float sum;
-        const bool done = need_mask ? block_row_p_chunked<true, BF16>(scol, rel_lim, sl2, -f, sum)
-                                    : block_row_p_chunked<false, BF16>(scol, rel_lim, sl2, -f,
-                                                                       sum);
-        if (done) {
-          pmx = fmaxf(pmx, sum);
-          l += sum;
-          return;
-        }
-      }
-    }
-    // two passes over S in tensor memory: the row max (and the frame test) first, then P
-    const float mx = need_mask ? block_row_max<true>(scol, rel_lim)
-                               : block_row_max<false>(scol, rel_lim);
-    float alpha;
-    if (frame_test(mx, alpha) && o_live) {
-      rescale_o(alpha);
-      tmem_wait_st();
-    }
-    const float nf = -f;
-    pmx = fmaxf(pmx, ex2(fmaf(mx, sl2, nf)));
-    l += need_mask ? block_row_exp<true, BF16>(scol, rel_lim, sl2, nf)
-                   : block_row_exp<false, BF16>(scol, rel_lim, sl2, nf);
+  const bool first = __any_sync(0xffffffffu, f == -INFINITY);
+  float s[kBN];
+  if (need_mask)
+    block_row_scores<true>(scol, rel_lim, s);
+  else
+    block_row_scores<false>(scol, rel_lim, s);
+  float sum = 0.f;
+  bool done = false;
+  if (!first) {
+    sum = block_row_exp_regs<BF16>(scol, s, sl2, -f);
+    done = !__any_sync(0xffffffffu, sum > kSumTrigger);
   }
+  if (done) {
+    pmx = fmaxf(pmx, sum);
+  } else {
+    const float mx = row_max_regs(s);
+    float alpha;
+    const bool any = frame_test(mx, alpha);
+    if (any || first) {
+      sum = block_row_exp_regs<BF16>(scol, s, sl2, -f);
+      if (any && o_live) rescale_o(alpha);
+    }
+    pmx = fmaxf(pmx, ex2(fmaf(mx, sl2, -f)));  // -inf keys (a masked row) give 0
+  }
+  l += sum;
 }
 
 // One q4_0 dequant item: the 32 elements of block blk of key row t of a raw tile (nibble rows of
@@ -617,290 +479,339 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-    }
-    bool ok = true;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(kBarQFull), (hasB ? 2 : 1) * C::kQBytes);
-      for (int t = 0; t < (hasB ? 2 : 1); ++t)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (kBM * 128), &tm_q,
-                      bar(kBarQFull), c * 64, t ? q0B : q0A, b * args.Hq + h);
-    }
-    // tiles in the order the MMA first uses them: K0, V0, K1, V1, ...; dense tiles go by TMA
-    // straight into the ring, q4_0 tiles (nibbles + scales) into the raw stages
-    int n = 0;  // ring tiles
-    int r = 0;  // raw q4_0 tiles
-    auto produce = [&](bool is_v, int j) {
-      if (!ok) return;
-      if (!(is_v ? VQ4 : KQ4)) {
-        const int s = n % C::kStages;
+  // Roles by warpgroup first.  With a q4_0 side (sixteen warps) the two softmax warpgroups
+  // raise their registers to 168 a thread and the other two lower theirs to 88 (setmaxnreg is
+  // executed by whole warpgroups, so warps 0-3 take it together before splitting into producer,
+  // issuer and dequant), and the softmax keeps a block's 128 scores in registers as with dense
+  // K/V; 2 x 128 x 168 + 2 x 128 x 88 is exactly the 65 536 registers the launch reserved.
+  if (warp < 4 || warp >= 12) {
+    if constexpr (C::kWide) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+    if (warp == 0) {
+      // ---------------------------------------------------------------- producer
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+      }
+      bool ok = true;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(kBarQFull), (hasB ? 2 : 1) * C::kQBytes);
+        for (int t = 0; t < (hasB ? 2 : 1); ++t)
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (kBM * 128), &tm_q,
+                        bar(kBarQFull), c * 64, t ? q0B : q0A, b * args.Hq + h);
+      }
+      // tiles in the order the MMA first uses them: K0, V0, K1, V1, ...; dense tiles go by TMA
+      // straight into the ring, q4_0 tiles (nibbles + scales) into the raw stages
+      int n = 0;  // ring tiles
+      int r = 0;  // raw q4_0 tiles
+      auto produce = [&](bool is_v, int j) {
+        if (!ok) return;
+        if (!(is_v ? VQ4 : KQ4)) {
+          const int s = n % C::kStages;
+          if (lane == 0) {
+            if (n >= C::kStages)
+              ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                             &g_prefill_error);
+            if (ok) {
+              mbar_arrive_expect_tx(bar(kBarRingFull + s), C::kTileBytes);
+              const uint32_t dst = sbase + C::kOffRing + s * C::kTileBytes;
+              for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(dst + c * (kBN * 128), is_v ? &tm_v : &tm_k, bar(kBarRingFull + s),
+                            c * 64, j * kBN, b * args.Hkv + g);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        } else {
+          const int s = r % C::kRawStages;
+          if (r >= C::kRawStages) {
+            if (lane == 0)
+              ok = mbar_wait(bar(kBarRawEmpty + s), ((r / C::kRawStages) - 1) & 1, abort_flag,
+                             &g_prefill_error);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) return;
+          }
+          const uint32_t dst = sbase + C::kOffRaw + s * C::kRawBytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(kBarRawFull + s), C::kRawNib);
+            tma_load_3d(dst, is_v ? &tm_v : &tm_k, bar(kBarRawFull + s), 0, j * kBN,
+                        b * args.Hkv + g);
+          }
+          // scales: one 4- or 8-byte row per key, zero-filled past Sk
+          const uint8_t* sp = is_v ? args.v_scale : args.k_scale;
+          for (int row = lane; row < kBN; row += 32) {
+            const int key = j * kBN + row;
+            const bool in = key < args.Sk;
+            const uint8_t* src =
+                sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Scap + (in ? key : 0)) *
+                         C::kScaleRow;
+            const uint32_t d = dst + C::kRawNib + row * C::kScaleRow;
+            if (C::kScaleRow == 8)
+              cp_async_8(d, src, in ? 8u : 0u);
+            else
+              cp_async_4(d, src, in ? 4u : 0u);
+          }
+          cp_async_mbar_arrive_noinc(bar(kBarRawFull + s));
+          ++r;
+        }
+        ++n;
+      };
+      // dense K/V: one slot per block step, K tile in its first stage, V tile in its second
+      int pg = 0;  // slots filled
+      auto produce_pair = [&](int kj, int vj) {
+        if (!ok) return;
+        const int p = pg % C::kSlots;
         if (lane == 0) {
-          if (n >= C::kStages)
-            ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+          if (pg >= C::kSlots)
+            ok = mbar_wait(bar(kBarRingEmpty + p), ((pg / C::kSlots) - 1) & 1, abort_flag,
                            &g_prefill_error);
           if (ok) {
-            mbar_arrive_expect_tx(bar(kBarRingFull + s), C::kTileBytes);
-            const uint32_t dst = sbase + C::kOffRing + s * C::kTileBytes;
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d(dst + c * (kBN * 128), is_v ? &tm_v : &tm_k, bar(kBarRingFull + s),
-                          c * 64, j * kBN, b * args.Hkv + g);
+            mbar_arrive_expect_tx(bar(kBarRingFull + p),
+                                  ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
+            const uint32_t dst = sbase + C::kOffRing + 2 * p * C::kTileBytes;
+            for (int c = 0; c < D / 64; ++c) {
+              if (kj >= 0)
+                tma_load_3d(dst + c * (kBN * 128), &tm_k, bar(kBarRingFull + p), c * 64, kj * kBN,
+                            b * args.Hkv + g);
+              if (vj >= 0)
+                tma_load_3d(dst + C::kTileBytes + c * (kBN * 128), &tm_v, bar(kBarRingFull + p),
+                            c * 64, vj * kBN, b * args.Hkv + g);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (ok) ++pg;
+      };
+      if constexpr (C::kPaired) {
+        produce_pair(0, -1);
+        for (int j = 0; j < nbmax; ++j) produce_pair(j + 1 < nbmax ? j + 1 : -1, j);
       } else {
-        const int s = r % C::kRawStages;
-        if (r >= C::kRawStages) {
-          if (lane == 0)
-            ok = mbar_wait(bar(kBarRawEmpty + s), ((r / C::kRawStages) - 1) & 1, abort_flag,
-                           &g_prefill_error);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) return;
+        for (int j = 0; j < nbmax; ++j) {
+          produce(false, j);
+          produce(true, j);
         }
-        const uint32_t dst = sbase + C::kOffRaw + s * C::kRawBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(kBarRawFull + s), C::kRawNib);
-          tma_load_3d(dst, is_v ? &tm_v : &tm_k, bar(kBarRawFull + s), 0, j * kBN,
-                      b * args.Hkv + g);
-        }
-        // scales: one 4- or 8-byte row per key, zero-filled past Sk
-        const uint8_t* sp = is_v ? args.v_scale : args.k_scale;
-        for (int row = lane; row < kBN; row += 32) {
-          const int key = j * kBN + row;
-          const bool in = key < args.Sk;
-          const uint8_t* src =
-              sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Scap + (in ? key : 0)) *
-                       C::kScaleRow;
-          const uint32_t d = dst + C::kRawNib + row * C::kScaleRow;
-          if (C::kScaleRow == 8)
-            cp_async_8(d, src, in ? 8u : 0u);
-          else
-            cp_async_4(d, src, in ? 4u : 0u);
-        }
-        cp_async_mbar_arrive_noinc(bar(kBarRawFull + s));
-        ++r;
       }
-      ++n;
-    };
-    // dense K/V: one slot per block step, K tile in its first stage, V tile in its second
-    int pg = 0;  // slots filled
-    auto produce_pair = [&](int kj, int vj) {
-      if (!ok) return;
-      const int p = pg % C::kSlots;
+      if (!ok && lane == 0) {
+        // let copies already issued land before the CTA's shared memory goes away: the last
+        // dense tiles sent into the ring and the last raw q4_0 tiles
+        volatile int never = 0;
+        if constexpr (C::kPaired) {
+          for (int i = max(0, pg - C::kSlots); i < pg; ++i)
+            mbar_wait(bar(kBarRingFull + i % C::kSlots), (i / C::kSlots) & 1, &never, nullptr,
+                      kWaitLimitNs);
+        }
+        for (int i = max(0, n - C::kStages); i < n; ++i)
+          if (!((i & 1) ? VQ4 : KQ4))
+            mbar_wait(bar(kBarRingFull + i % C::kStages), (i / C::kStages) & 1, &never, nullptr,
+                      kWaitLimitNs);
+        if constexpr (C::kAnyQ4) {
+          for (int i = max(0, r - C::kRawStages); i < r; ++i)
+            mbar_wait(bar(kBarRawFull + i % C::kRawStages), (i / C::kRawStages) & 1, &never,
+                      nullptr, kWaitLimitNs);
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        if (pg >= C::kSlots)
-          ok = mbar_wait(bar(kBarRingEmpty + p), ((pg / C::kSlots) - 1) & 1, abort_flag,
-                         &g_prefill_error);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(kBarRingFull + p),
-                                ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
-          const uint32_t dst = sbase + C::kOffRing + 2 * p * C::kTileBytes;
-          for (int c = 0; c < D / 64; ++c) {
-            if (kj >= 0)
-              tma_load_3d(dst + c * (kBN * 128), &tm_k, bar(kBarRingFull + p), c * 64, kj * kBN,
-                          b * args.Hkv + g);
-            if (vj >= 0)
-              tma_load_3d(dst + C::kTileBytes + c * (kBN * 128), &tm_v, bar(kBarRingFull + p),
-                          c * 64, vj * kBN, b * args.Hkv + g);
-          }
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (ok) ++pg;
-    };
-    if constexpr (C::kPaired) {
-      produce_pair(0, -1);
-      for (int j = 0; j < nbmax; ++j) produce_pair(j + 1 < nbmax ? j + 1 : -1, j);
-    } else {
-      for (int j = 0; j < nbmax; ++j) {
-        produce(false, j);
-        produce(true, j);
-      }
-    }
-    if (!ok && lane == 0) {
-      // let copies already issued land before the CTA's shared memory goes away: the last
-      // dense tiles sent into the ring and the last raw q4_0 tiles
-      volatile int never = 0;
-      if constexpr (C::kPaired) {
-        for (int i = max(0, pg - C::kSlots); i < pg; ++i)
-          mbar_wait(bar(kBarRingFull + i % C::kSlots), (i / C::kSlots) & 1, &never, nullptr,
-                    kWaitLimitNs);
-      }
-      for (int i = max(0, n - C::kStages); i < n; ++i)
-        if (!((i & 1) ? VQ4 : KQ4))
-          mbar_wait(bar(kBarRingFull + i % C::kStages), (i / C::kStages) & 1, &never, nullptr,
-                    kWaitLimitNs);
-      if constexpr (C::kAnyQ4) {
-        for (int i = max(0, r - C::kRawStages); i < r; ++i)
-          mbar_wait(bar(kBarRawFull + i % C::kRawStages), (i / C::kRawStages) & 1, &never,
-                    nullptr, kWaitLimitNs);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_f16(kBM, kBN, BF16, false);
-      constexpr uint32_t idesc_pv = make_idesc_f16(kBM, D, BF16, true);
-      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, &g_prefill_error);
-      tc_fence_after();
-      int n = 0;
-      auto acquire = [&]() -> int {
-        const int s = n % C::kStages;
-        if (ok) ok = mbar_wait(bar(kBarRingFull + s), (n / C::kStages) & 1, abort_flag,
-                               &g_prefill_error);
+        constexpr uint32_t idesc_qk = make_idesc_f16(kBM, kBN, BF16, false);
+        constexpr uint32_t idesc_pv = make_idesc_f16(kBM, D, BF16, true);
+        bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag, &g_prefill_error);
         tc_fence_after();
-        ++n;
-        return s;
-      };
-      auto release = [&](int s) { mma_commit(bar(kBarRingEmpty + s)); };
-      // QK of query tile t into S buffer sb (tile t's own, except in the alternating mode)
-      auto issue_qk = [&](int t, int s, int sb) {
-        const uint32_t qaddr = sbase + C::kOffQ + t * C::kQBytes;
-        const uint32_t kaddr = sbase + C::kOffRing + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          mma_ss(tmem + col_s(sb), make_sdesc_sw128(qaddr + off, 16, 1024),
-                 make_sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(kBarSFull + sb));
-      };
-      auto issue_pv = [&](int t, int j, int s, int nb_t) {
-        ok = ok && mbar_wait(bar(kBarPReady + t), j & 1, abort_flag, &g_prefill_error);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
-        const uint32_t ocol = t ? C::kColO1 : C::kColO0;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + ocol, tmem + col_s(t) + kk * 8,
-                 make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        if (j == nb_t - 1) mma_commit(bar(kBarODone + t));
-      };
-      // PV of block j of a lone query tile whose blocks alternate between the S buffers; tile
-      // B's O-done barrier, unused then, completes after every PV (the softmax waits for it
-      // before it rescales O)
-      auto issue_pv_alt = [&](int j, int s, int nb_t) {
-        const int sb = j & 1;
-        ok = ok && mbar_wait(bar(kBarPReady + sb), (j >> 1) & 1, abort_flag, &g_prefill_error);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + C::kColO0, tmem + col_s(sb) + kk * 8,
-                 make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(kBarODone + 1));
-        if (j == nb_t - 1) mma_commit(bar(kBarODone));
-      };
-      // order: QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage is
-      // acquired at the start of the step that first uses it and released after its last use
-      // (all in ring order).
-      if constexpr (C::kPaired) {
-        // one slot per step: V(j) in stage 2p + 1, K(j + 1) in stage 2p
-        int gn = 0;
-        auto acquire_g = [&]() -> int {
-          const int p = gn % C::kSlots;
-          if (ok) ok = mbar_wait(bar(kBarRingFull + p), (gn / C::kSlots) & 1, abort_flag,
+        int n = 0;
+        auto acquire = [&]() -> int {
+          const int s = n % C::kStages;
+          if (ok) ok = mbar_wait(bar(kBarRingFull + s), (n / C::kStages) & 1, abort_flag,
                                  &g_prefill_error);
           tc_fence_after();
-          ++gn;
-          return p;
+          ++n;
+          return s;
         };
-        if constexpr (ALT) {
-          // one query tile whose key blocks alternate between the two S buffers: QK(j + 2) goes
-          // into block j's buffer right after PV(j) has read P from it, so the softmax finds
-          // block j + 1's scores ready when it finishes block j.  Slot 0 holds K(0), slot g
-          // holds V(g - 1) and K(g).
-          int pvs = 0;  // the slot holding the V of the next PV
-          if (nbA > 0 && ok) {
+        auto release = [&](int s) { mma_commit(bar(kBarRingEmpty + s)); };
+        // QK of query tile t into S buffer sb (tile t's own, except in the alternating mode)
+        auto issue_qk = [&](int t, int s, int sb) {
+          const uint32_t qaddr = sbase + C::kOffQ + t * C::kQBytes;
+          const uint32_t kaddr = sbase + C::kOffRing + s * C::kTileBytes;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+            mma_ss(tmem + col_s(sb), make_sdesc_sw128(qaddr + off, 16, 1024),
+                   make_sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(kBarSFull + sb));
+        };
+        auto issue_pv = [&](int t, int j, int s, int nb_t) {
+          ok = ok && mbar_wait(bar(kBarPReady + t), j & 1, abort_flag, &g_prefill_error);
+          if (!ok) return;
+          tc_fence_after();
+          const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
+          const uint32_t ocol = t ? C::kColO1 : C::kColO0;
+  #pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + ocol, tmem + col_s(t) + kk * 8,
+                   make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          if (j == nb_t - 1) mma_commit(bar(kBarODone + t));
+        };
+        // PV of block j of a lone query tile whose blocks alternate between the S buffers; tile
+        // B's O-done barrier, unused then, completes after every PV (the softmax waits for it
+        // before it rescales O)
+        auto issue_pv_alt = [&](int j, int s, int nb_t) {
+          const int sb = j & 1;
+          ok = ok && mbar_wait(bar(kBarPReady + sb), (j >> 1) & 1, abort_flag, &g_prefill_error);
+          if (!ok) return;
+          tc_fence_after();
+          const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
+  #pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + C::kColO0, tmem + col_s(sb) + kk * 8,
+                   make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(kBarODone + 1));
+          if (j == nb_t - 1) mma_commit(bar(kBarODone));
+        };
+        // order: QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage is
+        // acquired at the start of the step that first uses it and released after its last use
+        // (all in ring order).
+        if constexpr (C::kPaired) {
+          // one slot per step: V(j) in stage 2p + 1, K(j + 1) in stage 2p
+          int gn = 0;
+          auto acquire_g = [&]() -> int {
+            const int p = gn % C::kSlots;
+            if (ok) ok = mbar_wait(bar(kBarRingFull + p), (gn / C::kSlots) & 1, abort_flag,
+                                   &g_prefill_error);
+            tc_fence_after();
+            ++gn;
+            return p;
+          };
+          if constexpr (ALT) {
+            // one query tile whose key blocks alternate between the two S buffers: QK(j + 2) goes
+            // into block j's buffer right after PV(j) has read P from it, so the softmax finds
+            // block j + 1's scores ready when it finishes block j.  Slot 0 holds K(0), slot g
+            // holds V(g - 1) and K(g).
+            int pvs = 0;  // the slot holding the V of the next PV
+            if (nbA > 0 && ok) {
+              const int p = acquire_g();
+              if (ok) {
+                issue_qk(0, 2 * p, 0);
+                release(p);
+                pvs = acquire_g();
+                if (ok && nbA > 1) issue_qk(0, 2 * pvs, 1);
+              }
+            }
+            for (int j = 0; j < nbA && ok; ++j) {
+              issue_pv_alt(j, 2 * pvs + 1, nbA);
+              if (!ok) break;
+              release(pvs);
+              if (j + 1 < nbA) {
+                pvs = acquire_g();
+                if (ok && j + 2 < nbA) issue_qk(0, 2 * pvs, j & 1);
+              }
+            }
+          } else {
+          if (nbmax > 0 && ok) {
             const int p = acquire_g();
             if (ok) {
-              issue_qk(0, 2 * p, 0);
-              release(p);
-              pvs = acquire_g();
-              if (ok && nbA > 1) issue_qk(0, 2 * pvs, 1);
+              if (nbA > 0) issue_qk(0, 2 * p, 0);
+              if (nbB > 0)
+                issue_qk(1, 2 * p, 1);  // tile B's softmax releases the slot
+              else
+                release(p);
             }
           }
-          for (int j = 0; j < nbA && ok; ++j) {
-            issue_pv_alt(j, 2 * pvs + 1, nbA);
+          for (int j = 0; j < nbmax && ok; ++j) {
+            const int p = acquire_g();
+            const bool next = j + 1 < nbmax;
             if (!ok) break;
-            release(pvs);
-            if (j + 1 < nbA) {
-              pvs = acquire_g();
-              if (ok && j + 2 < nbA) issue_qk(0, 2 * pvs, j & 1);
-            }
-          }
-        } else {
-        if (nbmax > 0 && ok) {
-          const int p = acquire_g();
-          if (ok) {
-            if (nbA > 0) issue_qk(0, 2 * p, 0);
-            if (nbB > 0)
-              issue_qk(1, 2 * p, 1);  // tile B's softmax releases the slot
+            if (j < nbA) issue_pv(0, j, 2 * p + 1, nbA);
+            if (!ok) break;
+            if (next && j + 1 < nbA) issue_qk(0, 2 * p, 0);
+            if (j < nbB) issue_pv(1, j, 2 * p + 1, nbB);
+            if (!ok) break;
+            if (next && j + 1 < nbB)
+              issue_qk(1, 2 * p, 1);
             else
               release(p);
           }
+          }
+        } else {
+        if (nbmax > 0 && ok) {
+          const int sK = acquire();
+          if (ok) {
+            if (nbA > 0) issue_qk(0, sK, 0);
+            if (nbB > 0) issue_qk(1, sK, 1);
+            release(sK);
+          }
         }
         for (int j = 0; j < nbmax && ok; ++j) {
-          const int p = acquire_g();
+          // both ring waits of the step sit next to the P_A wait: an mbarrier wait issued while
+          // the MMA queue is short stalls the issue of the next MMAs, so the waits are grouped
+          // where they cost one stall instead of one per wait
+          const int sV = acquire();
           const bool next = j + 1 < nbmax;
+          const int sK = next ? acquire() : 0;
           if (!ok) break;
-          if (j < nbA) issue_pv(0, j, 2 * p + 1, nbA);
+          if (j < nbA) issue_pv(0, j, sV, nbA);
           if (!ok) break;
-          if (next && j + 1 < nbA) issue_qk(0, 2 * p, 0);
-          if (j < nbB) issue_pv(1, j, 2 * p + 1, nbB);
+          if (next && j + 1 < nbA) issue_qk(0, sK, 0);
+          if (j < nbB) issue_pv(1, j, sV, nbB);
           if (!ok) break;
-          if (next && j + 1 < nbB)
-            issue_qk(1, 2 * p, 1);
-          else
-            release(p);
+          release(sV);
+          if (next) {
+            if (j + 1 < nbB) issue_qk(1, sK, 1);
+            release(sK);
+          }
         }
         }
-      } else {
-      if (nbmax > 0 && ok) {
-        const int sK = acquire();
-        if (ok) {
-          if (nbA > 0) issue_qk(0, sK, 0);
-          if (nbB > 0) issue_qk(1, sK, 1);
-          release(sK);
+        if (!ok) {
+          // wait until every MMA issued so far has finished before TMEM is released
+          volatile int never = 0;
+          mma_commit(bar(kBarDrain));
+          mbar_wait(bar(kBarDrain), 0, &never, nullptr, kWaitLimitNs);
         }
       }
-      for (int j = 0; j < nbmax && ok; ++j) {
-        // both ring waits of the step sit next to the P_A wait: an mbarrier wait issued while
-        // the MMA queue is short stalls the issue of the next MMAs, so the waits are grouped
-        // where they cost one stall instead of one per wait
-        const int sV = acquire();
-        const bool next = j + 1 < nbmax;
-        const int sK = next ? acquire() : 0;
-        if (!ok) break;
-        if (j < nbA) issue_pv(0, j, sV, nbA);
-        if (!ok) break;
-        if (next && j + 1 < nbA) issue_qk(0, sK, 0);
-        if (j < nbB) issue_pv(1, j, sV, nbB);
-        if (!ok) break;
-        release(sV);
-        if (next) {
-          if (j + 1 < nbB) issue_qk(1, sK, 1);
-          release(sK);
+    } else if constexpr (C::kAnyQ4) {
+      if (C::is_dq_warp(warp)) {
+        // -------------------------------------------------------------- q4_0 dequant
+        // the dequant threads share out each raw tile's (key row, block) items and expand them
+        // into the 128B-swizzled f16/bf16 ring stage
+        const int u = C::dq_index(warp, lane);
+        const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
+        bool ok = true;
+        const int ntiles = 2 * nbmax;
+        int r = 0;  // raw q4_0 tiles consumed
+        for (int n = 0; n < ntiles; ++n) {
+          if (!((n & 1) ? VQ4 : KQ4)) continue;  // a dense tile: the producer's TMA fills it
+          const int rs = r % C::kRawStages;
+          const int s = n % C::kStages;
+          ok = mbar_wait(bar(kBarRawFull + rs), (r / C::kRawStages) & 1, abort_flag,
+                         &g_prefill_error);
+          if (ok && n >= C::kStages)
+            ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                           &g_prefill_error);
+          if (!ok) break;
+          const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
+          uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
+          // items (key row t, 32-element block blk) of the tile, rows fastest; unrolled so that
+          // the items' shared-memory loads overlap
+          constexpr int kItems = kBN * (D / 32);
+  #pragma unroll
+          for (int k = 0; k < (kItems + C::kDqThreads - 1) / C::kDqThreads; ++k) {
+            const int it = u + k * C::kDqThreads;
+            if (kItems % C::kDqThreads == 0 || it < kItems)
+              dequant_item<D, BF16, C::kNibRow, C::kScaleRow, C::kRawNib>(raw, dst, it % kBN,
+                                                                          it / kBN, mg);
+          }
+          // generic-proxy writes must be visible to the tensor core's async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(bar(kBarRingFull + s));
+          mbar_arrive(bar(kBarRawEmpty + rs));
+          ++r;
         }
       }
-      }
-      if (!ok) {
-        // wait until every MMA issued so far has finished before TMEM is released
-        volatile int never = 0;
-        mma_commit(bar(kBarDrain));
-        mbar_wait(bar(kBarDrain), 0, &never, nullptr, kWaitLimitNs);
-      }
+  
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else {
+    if constexpr (C::kWide) asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
     // ---------------------------------------------------------------- softmax rows
     const int t = (warp >= 8) ? 1 : 0;  // query tile
     const int nb = t ? nbB : nbA;
@@ -946,10 +857,10 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
           mbar_wait(bar(kBarODone + 1), (j - 1) & 1, abort_flag, &g_prefill_error);
           tc_fence_after();
         };
-        softmax_block<D, BF16, !C::kWide, C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > 0,
+        softmax_block<D, BF16>(scol, ocol, need_mask, rel_lim, sl2, j > 0,
                                                     f, l, nres, pmx, wait_pv);
       } else {
-        softmax_block<D, BF16, !C::kWide, C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > 0,
+        softmax_block<D, BF16>(scol, ocol, need_mask, rel_lim, sl2, j > 0,
                                                     f, l, nres, pmx);
       }
       tmem_wait_st();
@@ -989,45 +900,6 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
         args.rescale_count[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = nres;
       if (store && args.p_max)
         args.p_max[static_cast<int64_t>(b * args.Hq + h) * args.Sq + qrow] = pmx;
-    }
-  } else if constexpr (C::kAnyQ4) {
-    if (C::is_dq_warp(warp)) {
-      // -------------------------------------------------------------- q4_0 dequant
-      // the dequant threads share out each raw tile's (key row, block) items and expand them
-      // into the 128B-swizzled f16/bf16 ring stage
-      const int u = C::dq_index(warp, lane);
-      const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
-      bool ok = true;
-      const int ntiles = 2 * nbmax;
-      int r = 0;  // raw q4_0 tiles consumed
-      for (int n = 0; n < ntiles; ++n) {
-        if (!((n & 1) ? VQ4 : KQ4)) continue;  // a dense tile: the producer's TMA fills it
-        const int rs = r % C::kRawStages;
-        const int s = n % C::kStages;
-        ok = mbar_wait(bar(kBarRawFull + rs), (r / C::kRawStages) & 1, abort_flag,
-                       &g_prefill_error);
-        if (ok && n >= C::kStages)
-          ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
-                         &g_prefill_error);
-        if (!ok) break;
-        const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
-        uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
-        // items (key row t, 32-element block blk) of the tile, rows fastest; unrolled so that
-        // the items' shared-memory loads overlap
-        constexpr int kItems = kBN * (D / 32);
-#pragma unroll
-        for (int k = 0; k < (kItems + C::kDqThreads - 1) / C::kDqThreads; ++k) {
-          const int it = u + k * C::kDqThreads;
-          if (kItems % C::kDqThreads == 0 || it < kItems)
-            dequant_item<D, BF16, C::kNibRow, C::kScaleRow, C::kRawNib>(raw, dst, it % kBN,
-                                                                        it / kBN, mg);
-        }
-        // generic-proxy writes must be visible to the tensor core's async proxy
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(bar(kBarRingFull + s));
-        mbar_arrive(bar(kBarRawEmpty + rs));
-        ++r;
-      }
     }
   }
 
@@ -1380,305 +1252,354 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int nseg = *seg_count;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-    }
-    bool ok = true;
-    // tiles in the order the MMA first uses them: K0, V0, K1, V1, ... of each segment; dense
-    // tiles go by TMA straight into the ring, q4_0 tiles (nibbles + scales) into the raw stages
-    int n = 0;   // ring tiles
-    int r = 0;   // raw q4_0 tiles
-    int qn = 0;  // Q loads issued
-    int b = 0, g = 0;  // the segment's batch and kv head
-    auto produce = [&](bool is_v, int j) {
-      if (!ok) return;
-      if (!(is_v ? VQ4 : KQ4)) {
-        const int s = n % C::kStages;
+  // Roles by warpgroup first.  With a q4_0 side (sixteen warps) the two softmax warpgroups
+  // raise their registers to 168 a thread and the other two lower theirs to 88 (setmaxnreg is
+  // executed by whole warpgroups, so warps 0-3 take it together before splitting into producer,
+  // issuer and dequant), and the softmax keeps a block's 128 scores in registers as with dense
+  // K/V; 2 x 128 x 168 + 2 x 128 x 88 is exactly the 65 536 registers the launch reserved.
+  if (warp < 4 || warp >= 12) {
+    if constexpr (C::kWide) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+    if (warp == 0) {
+      // ---------------------------------------------------------------- producer
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+      }
+      bool ok = true;
+      // tiles in the order the MMA first uses them: K0, V0, K1, V1, ... of each segment; dense
+      // tiles go by TMA straight into the ring, q4_0 tiles (nibbles + scales) into the raw stages
+      int n = 0;   // ring tiles
+      int r = 0;   // raw q4_0 tiles
+      int qn = 0;  // Q loads issued
+      int b = 0, g = 0;  // the segment's batch and kv head
+      auto produce = [&](bool is_v, int j) {
+        if (!ok) return;
+        if (!(is_v ? VQ4 : KQ4)) {
+          const int s = n % C::kStages;
+          if (lane == 0) {
+            if (n >= C::kStages)
+              ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                             &g_prefill_error);
+            if (ok) {
+              mbar_arrive_expect_tx(bar(kBarRingFull + s), C::kTileBytes);
+              const uint32_t dst = sbase + C::kOffRing + s * C::kTileBytes;
+              for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(dst + c * (kBN * 128), is_v ? &tm_v : &tm_k, bar(kBarRingFull + s),
+                            c * 64, j * kBN, b * args.Hkv + g);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        } else {
+          const int s = r % C::kRawStages;
+          if (r >= C::kRawStages) {
+            if (lane == 0)
+              ok = mbar_wait(bar(kBarRawEmpty + s), ((r / C::kRawStages) - 1) & 1, abort_flag,
+                             &g_prefill_error);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) return;
+          }
+          const uint32_t dst = sbase + C::kOffRaw + s * C::kRawBytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(kBarRawFull + s), C::kRawNib);
+            tma_load_3d(dst, is_v ? &tm_v : &tm_k, bar(kBarRawFull + s), 0, j * kBN,
+                        b * args.Hkv + g);
+          }
+          // scales: one 4- or 8-byte row per key, zero-filled past Sk
+          const uint8_t* sp = is_v ? args.v_scale : args.k_scale;
+          for (int row = lane; row < kBN; row += 32) {
+            const int key = j * kBN + row;
+            const bool in = key < args.Sk;
+            const uint8_t* src =
+                sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Scap + (in ? key : 0)) *
+                         C::kScaleRow;
+            const uint32_t d = dst + C::kRawNib + row * C::kScaleRow;
+            if (C::kScaleRow == 8)
+              cp_async_8(d, src, in ? 8u : 0u);
+            else
+              cp_async_4(d, src, in ? 4u : 0u);
+          }
+          cp_async_mbar_arrive_noinc(bar(kBarRawFull + s));
+          ++r;
+        }
+        ++n;
+      };
+      // dense K/V: one slot per block step, K tile in its first stage, V tile in its second
+      int pg = 0;  // slots filled
+      auto produce_pair = [&](int kj, int vj) {
+        if (!ok) return;
+        const int p = pg % C::kSlots;
         if (lane == 0) {
-          if (n >= C::kStages)
-            ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+          if (pg >= C::kSlots)
+            ok = mbar_wait(bar(kBarRingEmpty + p), ((pg / C::kSlots) - 1) & 1, abort_flag,
                            &g_prefill_error);
           if (ok) {
-            mbar_arrive_expect_tx(bar(kBarRingFull + s), C::kTileBytes);
-            const uint32_t dst = sbase + C::kOffRing + s * C::kTileBytes;
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d(dst + c * (kBN * 128), is_v ? &tm_v : &tm_k, bar(kBarRingFull + s),
-                          c * 64, j * kBN, b * args.Hkv + g);
+            mbar_arrive_expect_tx(bar(kBarRingFull + p),
+                                  ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
+            const uint32_t dst = sbase + C::kOffRing + 2 * p * C::kTileBytes;
+            for (int c = 0; c < D / 64; ++c) {
+              if (kj >= 0)
+                tma_load_3d(dst + c * (kBN * 128), &tm_k, bar(kBarRingFull + p), c * 64, kj * kBN,
+                            b * args.Hkv + g);
+              if (vj >= 0)
+                tma_load_3d(dst + C::kTileBytes + c * (kBN * 128), &tm_v, bar(kBarRingFull + p),
+                            c * 64, vj * kBN, b * args.Hkv + g);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      } else {
-        const int s = r % C::kRawStages;
-        if (r >= C::kRawStages) {
-          if (lane == 0)
-            ok = mbar_wait(bar(kBarRawEmpty + s), ((r / C::kRawStages) - 1) & 1, abort_flag,
-                           &g_prefill_error);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) return;
-        }
-        const uint32_t dst = sbase + C::kOffRaw + s * C::kRawBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(kBarRawFull + s), C::kRawNib);
-          tma_load_3d(dst, is_v ? &tm_v : &tm_k, bar(kBarRawFull + s), 0, j * kBN,
-                      b * args.Hkv + g);
-        }
-        // scales: one 4- or 8-byte row per key, zero-filled past Sk
-        const uint8_t* sp = is_v ? args.v_scale : args.k_scale;
-        for (int row = lane; row < kBN; row += 32) {
-          const int key = j * kBN + row;
-          const bool in = key < args.Sk;
-          const uint8_t* src =
-              sp + (static_cast<int64_t>(b * args.Hkv + g) * args.Scap + (in ? key : 0)) *
-                       C::kScaleRow;
-          const uint32_t d = dst + C::kRawNib + row * C::kScaleRow;
-          if (C::kScaleRow == 8)
-            cp_async_8(d, src, in ? 8u : 0u);
-          else
-            cp_async_4(d, src, in ? 4u : 0u);
-        }
-        cp_async_mbar_arrive_noinc(bar(kBarRawFull + s));
-        ++r;
-      }
-      ++n;
-    };
-    // dense K/V: one slot per block step, K tile in its first stage, V tile in its second
-    int pg = 0;  // slots filled
-    auto produce_pair = [&](int kj, int vj) {
-      if (!ok) return;
-      const int p = pg % C::kSlots;
-      if (lane == 0) {
-        if (pg >= C::kSlots)
-          ok = mbar_wait(bar(kBarRingEmpty + p), ((pg / C::kSlots) - 1) & 1, abort_flag,
-                         &g_prefill_error);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(kBarRingFull + p),
-                                ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
-          const uint32_t dst = sbase + C::kOffRing + 2 * p * C::kTileBytes;
-          for (int c = 0; c < D / 64; ++c) {
-            if (kj >= 0)
-              tma_load_3d(dst + c * (kBN * 128), &tm_k, bar(kBarRingFull + p), c * 64, kj * kBN,
-                          b * args.Hkv + g);
-            if (vj >= 0)
-              tma_load_3d(dst + C::kTileBytes + c * (kBN * 128), &tm_v, bar(kBarRingFull + p),
-                          c * 64, vj * kBN, b * args.Hkv + g);
-          }
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (ok) ++pg;
-    };
-    for (int sidx = 0; sidx < nseg && ok; ++sidx) {
-      const SegS sg = segs[sidx];
-      const bool hasB = sg.q0A + kBM < args.Sq;
-      b = sg.b;
-      g = sg.h / (args.Hq / args.Hkv);
-      // the segment's Q tiles, once the previous segment's last QK MMA has read the previous ones
-      if (lane == 0) {
-        if (sidx > 0)
-          ok = mbar_wait(bar(kBarQEmpty), (sidx - 1) & 1, abort_flag, &g_prefill_error);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(kBarQFull), (hasB ? 2 : 1) * C::kQBytes);
-          for (int t = 0; t < (hasB ? 2 : 1); ++t)
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (kBM * 128), &tm_q,
-                          bar(kBarQFull), c * 64, sg.q0A + t * kBM, sg.b * args.Hq + sg.h);
-          ++qn;
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if constexpr (C::kPaired) {
-        produce_pair(sg.j0, -1);
-        for (int j = sg.j0; j < sg.j1; ++j) produce_pair(j + 1 < sg.j1 ? j + 1 : -1, j);
-      } else {
-      for (int j = sg.j0; j < sg.j1; ++j) {
-        if constexpr (KQ4 && VQ4) {
-          if (args.app_flags != nullptr && ok && j >= args.app_j_lo &&
-              j < args.app_j_lo + args.app_nb) {
-            // the block holds appended tokens: wait until phase 1 has stored them
-            ok = app_wait(args.app_flags + (b * args.Hkv + g) * args.app_nb + (j - args.app_j_lo),
-                          abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-          }
-        }
-        produce(false, j);
-        produce(true, j);
-      }
-      }
-    }
-    if (!ok && lane == 0) {
-      // let copies already issued land before the CTA's shared memory goes away: the last
-      // Q tiles, the last dense tiles sent into the ring and the last raw q4_0 tiles
-      volatile int never = 0;
-      if (qn > 0)
-        mbar_wait(bar(kBarQFull), (qn - 1) & 1, &never, nullptr, kWaitLimitNs);
-      if constexpr (C::kPaired) {
-        for (int i = max(0, pg - C::kSlots); i < pg; ++i)
-          mbar_wait(bar(kBarRingFull + i % C::kSlots), (i / C::kSlots) & 1, &never, nullptr,
-                    kWaitLimitNs);
-      }
-      for (int i = max(0, n - C::kStages); i < n; ++i)
-        if (!((i & 1) ? VQ4 : KQ4))
-          mbar_wait(bar(kBarRingFull + i % C::kStages), (i / C::kStages) & 1, &never, nullptr,
-                    kWaitLimitNs);
-      if constexpr (C::kAnyQ4) {
-        for (int i = max(0, r - C::kRawStages); i < r; ++i)
-          mbar_wait(bar(kBarRawFull + i % C::kRawStages), (i / C::kRawStages) & 1, &never,
-                    nullptr, kWaitLimitNs);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_f16(kBM, kBN, BF16, false);
-      constexpr uint32_t idesc_pv = make_idesc_f16(kBM, D, BF16, true);
-      bool ok = true;
-      int n = 0;
-      int prA = 0, prB = 0;    // P-ready waits per tile before this segment (barrier phases)
-      int actA = 0, actB = 0;  // earlier segments in which the tile had blocks
-      int gn = 0;              // paired ring: slots taken
-      auto acquire_g = [&]() -> int {
-        const int p = gn % C::kSlots;
-        if (ok) ok = mbar_wait(bar(kBarRingFull + p), (gn / C::kSlots) & 1, abort_flag,
-                               &g_prefill_error);
-        tc_fence_after();
-        ++gn;
-        return p;
+        if (ok) ++pg;
       };
-      auto acquire = [&]() -> int {
-        const int s = n % C::kStages;
-        if (ok) ok = mbar_wait(bar(kBarRingFull + s), (n / C::kStages) & 1, abort_flag,
-                               &g_prefill_error);
-        tc_fence_after();
-        ++n;
-        return s;
-      };
-      auto release = [&](int s) { mma_commit(bar(kBarRingEmpty + s)); };
-      auto issue_qk = [&](int t, int s) {
-        const uint32_t qaddr = sbase + C::kOffQ + t * C::kQBytes;
-        const uint32_t kaddr = sbase + C::kOffRing + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          mma_ss(tmem + col_s(t), make_sdesc_sw128(qaddr + off, 16, 1024),
-                 make_sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(kBarSFull + t));
-      };
-      // PV of tile t for block j of a segment whose blocks for t are [j0, e_t); the P-ready
-      // phase of block j is (pb + j) & 1, pb = the tile's earlier P-ready waits - j0
-      auto issue_pv = [&](int t, int j, int s, int j0, int e_t, int pb) {
-        ok = ok && mbar_wait(bar(kBarPReady + t), (pb + j) & 1, abort_flag, &g_prefill_error);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
-        const uint32_t ocol = t ? C::kColO1 : C::kColO0;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + ocol, tmem + col_s(t) + kk * 8,
-                 make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
-                 (j > j0 || kk > 0) ? 1u : 0u);
-        if (j == e_t - 1) mma_commit(bar(kBarODone + t));
-      };
-      // per segment: QK_A(j0) QK_B(j0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage
-      // is acquired at the start of the step that first uses it and released after its last use
-      // (all in ring order).  Both ring waits of a step sit next to the P_A wait: an mbarrier
-      // wait issued while the MMA queue is short stalls the issue of the next MMAs, so the waits
-      // are grouped where they cost one stall instead of one per wait.
       for (int sidx = 0; sidx < nseg && ok; ++sidx) {
-        const int j0 = segs[sidx].j0, j1 = segs[sidx].j1;
-        const int eA = min(j1, segs[sidx].nbA);
-        const int eB = segs[sidx].q0A + kBM < args.Sq ? min(j1, segs[sidx].nbB) : 0;
-        ok = mbar_wait(bar(kBarQFull), sidx & 1, abort_flag, &g_prefill_error);
-        tc_fence_after();
-        if (!ok) break;
-        const int pbA = prA - j0, pbB = prB - j0;
+        const SegS sg = segs[sidx];
+        const bool hasB = sg.q0A + kBM < args.Sq;
+        b = sg.b;
+        g = sg.h / (args.Hq / args.Hkv);
+        // the segment's Q tiles, once the previous segment's last QK MMA has read the previous ones
+        if (lane == 0) {
+          if (sidx > 0)
+            ok = mbar_wait(bar(kBarQEmpty), (sidx - 1) & 1, abort_flag, &g_prefill_error);
+          if (ok) {
+            mbar_arrive_expect_tx(bar(kBarQFull), (hasB ? 2 : 1) * C::kQBytes);
+            for (int t = 0; t < (hasB ? 2 : 1); ++t)
+              for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(sbase + C::kOffQ + t * C::kQBytes + c * (kBM * 128), &tm_q,
+                            bar(kBarQFull), c * 64, sg.q0A + t * kBM, sg.b * args.Hq + sg.h);
+            ++qn;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if constexpr (C::kPaired) {
-          // one slot per step: V(j) in stage 2p + 1, K(j + 1) in stage 2p
-          {
-            const int p = acquire_g();
-            if (!ok) break;
-            if (j0 < eA) issue_qk(0, 2 * p);
-            if (j0 < eB)
-              issue_qk(1, 2 * p);  // tile B's softmax releases the slot
-            else
-              release(p);
-            if (j0 + 1 == j1) mma_commit(bar(kBarQEmpty));
-          }
-          if (j0 < eA && actA > 0)
-            ok = ok && mbar_wait(bar(kBarOFree + 0), (actA - 1) & 1, abort_flag,
-                                 &g_prefill_error);
-          if (j0 < eB && actB > 0)
-            ok = ok && mbar_wait(bar(kBarOFree + 1), (actB - 1) & 1, abort_flag,
-                                 &g_prefill_error);
-          for (int j = j0; j < j1 && ok; ++j) {
-            const int p = acquire_g();
-            const bool next = j + 1 < j1;
-            if (!ok) break;
-            if (j < eA) issue_pv(0, j, 2 * p + 1, j0, eA, pbA);
-            if (!ok) break;
-            if (next && j + 1 < eA) issue_qk(0, 2 * p);
-            if (j < eB) issue_pv(1, j, 2 * p + 1, j0, eB, pbB);
-            if (!ok) break;
-            if (next && j + 1 < eB)
-              issue_qk(1, 2 * p);
-            else
-              release(p);
-            if (next && j + 2 == j1) mma_commit(bar(kBarQEmpty));
-          }
+          produce_pair(sg.j0, -1);
+          for (int j = sg.j0; j < sg.j1; ++j) produce_pair(j + 1 < sg.j1 ? j + 1 : -1, j);
         } else {
-        {
-          const int sK = acquire();
-          if (!ok) break;
-          if (j0 < eA) issue_qk(0, sK);
-          if (j0 < eB) issue_qk(1, sK);
-          release(sK);
-          if (j0 + 1 == j1) mma_commit(bar(kBarQEmpty));  // no further QK reads these Q tiles
+        for (int j = sg.j0; j < sg.j1; ++j) {
+          if constexpr (KQ4 && VQ4) {
+            if (args.app_flags != nullptr && ok && j >= args.app_j_lo &&
+                j < args.app_j_lo + args.app_nb) {
+              // the block holds appended tokens: wait until phase 1 has stored them
+              ok = app_wait(args.app_flags + (b * args.Hkv + g) * args.app_nb + (j - args.app_j_lo),
+                            abort_flag);
+              ok = __all_sync(0xffffffffu, ok);
+            }
+          }
+          produce(false, j);
+          produce(true, j);
         }
-        // a tile's first PV of the segment overwrites O: wait until the previous segment's
-        // epilogue has read it (after this segment's first QKs are on their way)
-        if (j0 < eA && actA > 0)
-          ok = ok && mbar_wait(bar(kBarOFree + 0), (actA - 1) & 1, abort_flag, &g_prefill_error);
-        if (j0 < eB && actB > 0)
-          ok = ok && mbar_wait(bar(kBarOFree + 1), (actB - 1) & 1, abort_flag, &g_prefill_error);
-        for (int j = j0; j < j1 && ok; ++j) {
-          const int sV = acquire();
-          const bool next = j + 1 < j1;
-          const int sK = next ? acquire() : 0;
+        }
+      }
+      if (!ok && lane == 0) {
+        // let copies already issued land before the CTA's shared memory goes away: the last
+        // Q tiles, the last dense tiles sent into the ring and the last raw q4_0 tiles
+        volatile int never = 0;
+        if (qn > 0)
+          mbar_wait(bar(kBarQFull), (qn - 1) & 1, &never, nullptr, kWaitLimitNs);
+        if constexpr (C::kPaired) {
+          for (int i = max(0, pg - C::kSlots); i < pg; ++i)
+            mbar_wait(bar(kBarRingFull + i % C::kSlots), (i / C::kSlots) & 1, &never, nullptr,
+                      kWaitLimitNs);
+        }
+        for (int i = max(0, n - C::kStages); i < n; ++i)
+          if (!((i & 1) ? VQ4 : KQ4))
+            mbar_wait(bar(kBarRingFull + i % C::kStages), (i / C::kStages) & 1, &never, nullptr,
+                      kWaitLimitNs);
+        if constexpr (C::kAnyQ4) {
+          for (int i = max(0, r - C::kRawStages); i < r; ++i)
+            mbar_wait(bar(kBarRawFull + i % C::kRawStages), (i / C::kRawStages) & 1, &never,
+                      nullptr, kWaitLimitNs);
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = make_idesc_f16(kBM, kBN, BF16, false);
+        constexpr uint32_t idesc_pv = make_idesc_f16(kBM, D, BF16, true);
+        bool ok = true;
+        int n = 0;
+        int prA = 0, prB = 0;    // P-ready waits per tile before this segment (barrier phases)
+        int actA = 0, actB = 0;  // earlier segments in which the tile had blocks
+        int gn = 0;              // paired ring: slots taken
+        auto acquire_g = [&]() -> int {
+          const int p = gn % C::kSlots;
+          if (ok) ok = mbar_wait(bar(kBarRingFull + p), (gn / C::kSlots) & 1, abort_flag,
+                                 &g_prefill_error);
+          tc_fence_after();
+          ++gn;
+          return p;
+        };
+        auto acquire = [&]() -> int {
+          const int s = n % C::kStages;
+          if (ok) ok = mbar_wait(bar(kBarRingFull + s), (n / C::kStages) & 1, abort_flag,
+                                 &g_prefill_error);
+          tc_fence_after();
+          ++n;
+          return s;
+        };
+        auto release = [&](int s) { mma_commit(bar(kBarRingEmpty + s)); };
+        auto issue_qk = [&](int t, int s) {
+          const uint32_t qaddr = sbase + C::kOffQ + t * C::kQBytes;
+          const uint32_t kaddr = sbase + C::kOffRing + s * C::kTileBytes;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+            mma_ss(tmem + col_s(t), make_sdesc_sw128(qaddr + off, 16, 1024),
+                   make_sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(kBarSFull + t));
+        };
+        // PV of tile t for block j of a segment whose blocks for t are [j0, e_t); the P-ready
+        // phase of block j is (pb + j) & 1, pb = the tile's earlier P-ready waits - j0
+        auto issue_pv = [&](int t, int j, int s, int j0, int e_t, int pb) {
+          ok = ok && mbar_wait(bar(kBarPReady + t), (pb + j) & 1, abort_flag, &g_prefill_error);
+          if (!ok) return;
+          tc_fence_after();
+          const uint32_t vaddr = sbase + C::kOffRing + s * C::kTileBytes;
+          const uint32_t ocol = t ? C::kColO1 : C::kColO0;
+  #pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + ocol, tmem + col_s(t) + kk * 8,
+                   make_sdesc_sw128(vaddr + kk * (16 * 128), kBN * 128, 1024), idesc_pv,
+                   (j > j0 || kk > 0) ? 1u : 0u);
+          if (j == e_t - 1) mma_commit(bar(kBarODone + t));
+        };
+        // per segment: QK_A(j0) QK_B(j0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...  A K/V stage
+        // is acquired at the start of the step that first uses it and released after its last use
+        // (all in ring order).  Both ring waits of a step sit next to the P_A wait: an mbarrier
+        // wait issued while the MMA queue is short stalls the issue of the next MMAs, so the waits
+        // are grouped where they cost one stall instead of one per wait.
+        for (int sidx = 0; sidx < nseg && ok; ++sidx) {
+          const int j0 = segs[sidx].j0, j1 = segs[sidx].j1;
+          const int eA = min(j1, segs[sidx].nbA);
+          const int eB = segs[sidx].q0A + kBM < args.Sq ? min(j1, segs[sidx].nbB) : 0;
+          ok = mbar_wait(bar(kBarQFull), sidx & 1, abort_flag, &g_prefill_error);
+          tc_fence_after();
           if (!ok) break;
-          if (j < eA) issue_pv(0, j, sV, j0, eA, pbA);
-          if (!ok) break;
-          if (next && j + 1 < eA) issue_qk(0, sK);
-          if (j < eB) issue_pv(1, j, sV, j0, eB, pbB);
-          if (!ok) break;
-          release(sV);
-          if (next) {
-            if (j + 1 < eB) issue_qk(1, sK);
+          const int pbA = prA - j0, pbB = prB - j0;
+          if constexpr (C::kPaired) {
+            // one slot per step: V(j) in stage 2p + 1, K(j + 1) in stage 2p
+            {
+              const int p = acquire_g();
+              if (!ok) break;
+              if (j0 < eA) issue_qk(0, 2 * p);
+              if (j0 < eB)
+                issue_qk(1, 2 * p);  // tile B's softmax releases the slot
+              else
+                release(p);
+              if (j0 + 1 == j1) mma_commit(bar(kBarQEmpty));
+            }
+            if (j0 < eA && actA > 0)
+              ok = ok && mbar_wait(bar(kBarOFree + 0), (actA - 1) & 1, abort_flag,
+                                   &g_prefill_error);
+            if (j0 < eB && actB > 0)
+              ok = ok && mbar_wait(bar(kBarOFree + 1), (actB - 1) & 1, abort_flag,
+                                   &g_prefill_error);
+            for (int j = j0; j < j1 && ok; ++j) {
+              const int p = acquire_g();
+              const bool next = j + 1 < j1;
+              if (!ok) break;
+              if (j < eA) issue_pv(0, j, 2 * p + 1, j0, eA, pbA);
+              if (!ok) break;
+              if (next && j + 1 < eA) issue_qk(0, 2 * p);
+              if (j < eB) issue_pv(1, j, 2 * p + 1, j0, eB, pbB);
+              if (!ok) break;
+              if (next && j + 1 < eB)
+                issue_qk(1, 2 * p);
+              else
+                release(p);
+              if (next && j + 2 == j1) mma_commit(bar(kBarQEmpty));
+            }
+          } else {
+          {
+            const int sK = acquire();
+            if (!ok) break;
+            if (j0 < eA) issue_qk(0, sK);
+            if (j0 < eB) issue_qk(1, sK);
             release(sK);
-            if (j + 2 == j1) mma_commit(bar(kBarQEmpty));
+            if (j0 + 1 == j1) mma_commit(bar(kBarQEmpty));  // no further QK reads these Q tiles
+          }
+          // a tile's first PV of the segment overwrites O: wait until the previous segment's
+          // epilogue has read it (after this segment's first QKs are on their way)
+          if (j0 < eA && actA > 0)
+            ok = ok && mbar_wait(bar(kBarOFree + 0), (actA - 1) & 1, abort_flag, &g_prefill_error);
+          if (j0 < eB && actB > 0)
+            ok = ok && mbar_wait(bar(kBarOFree + 1), (actB - 1) & 1, abort_flag, &g_prefill_error);
+          for (int j = j0; j < j1 && ok; ++j) {
+            const int sV = acquire();
+            const bool next = j + 1 < j1;
+            const int sK = next ? acquire() : 0;
+            if (!ok) break;
+            if (j < eA) issue_pv(0, j, sV, j0, eA, pbA);
+            if (!ok) break;
+            if (next && j + 1 < eA) issue_qk(0, sK);
+            if (j < eB) issue_pv(1, j, sV, j0, eB, pbB);
+            if (!ok) break;
+            release(sV);
+            if (next) {
+              if (j + 1 < eB) issue_qk(1, sK);
+              release(sK);
+              if (j + 2 == j1) mma_commit(bar(kBarQEmpty));
+            }
+          }
+          }
+          if (j0 < eA) {
+            ++actA;
+            prA += eA - j0;
+          }
+          if (j0 < eB) {
+            ++actB;
+            prB += eB - j0;
           }
         }
-        }
-        if (j0 < eA) {
-          ++actA;
-          prA += eA - j0;
-        }
-        if (j0 < eB) {
-          ++actB;
-          prB += eB - j0;
+        if (!ok) {
+          // wait until every MMA issued so far has finished before TMEM is released
+          volatile int never = 0;
+          mma_commit(bar(kBarDrain));
+          mbar_wait(bar(kBarDrain), 0, &never, nullptr, kWaitLimitNs);
         }
       }
-      if (!ok) {
-        // wait until every MMA issued so far has finished before TMEM is released
-        volatile int never = 0;
-        mma_commit(bar(kBarDrain));
-        mbar_wait(bar(kBarDrain), 0, &never, nullptr, kWaitLimitNs);
+    } else if constexpr (C::kAnyQ4) {
+      if (C::is_dq_warp(warp)) {
+        // -------------------------------------------------------------- q4_0 dequant
+        // the dequant threads share out each raw tile's (key row, block) items and expand them
+        // into the 128B-swizzled f16/bf16 ring stage
+        const int u = C::dq_index(warp, lane);
+        const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
+        bool ok = true;
+        const int ntiles = static_cast<int>(2 * (t_end - t_begin));  // K and V of every step
+        int r = 0;  // raw q4_0 tiles consumed
+        for (int n = 0; n < ntiles; ++n) {
+          if (!((n & 1) ? VQ4 : KQ4)) continue;  // a dense tile: the producer's TMA fills it
+          const int rs = r % C::kRawStages;
+          const int s = n % C::kStages;
+          ok = mbar_wait(bar(kBarRawFull + rs), (r / C::kRawStages) & 1, abort_flag,
+                         &g_prefill_error);
+          if (ok && n >= C::kStages)
+            ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
+                           &g_prefill_error);
+          if (!ok) break;
+          const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
+          uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
+          // items (key row t, 32-element block blk) of the tile, rows fastest; unrolled so that
+          // the items' shared-memory loads overlap
+          constexpr int kItems = kBN * (D / 32);
+  #pragma unroll
+          for (int k = 0; k < (kItems + C::kDqThreads - 1) / C::kDqThreads; ++k) {
+            const int it = u + k * C::kDqThreads;
+            if (kItems % C::kDqThreads == 0 || it < kItems)
+              dequant_item<D, BF16, C::kNibRow, C::kScaleRow, C::kRawNib>(raw, dst, it % kBN,
+                                                                          it / kBN, mg);
+          }
+          // generic-proxy writes must be visible to the tensor core's async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(bar(kBarRingFull + s));
+          mbar_arrive(bar(kBarRawEmpty + rs));
+          ++r;
+        }
       }
+  
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else {
+    if constexpr (C::kWide) asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
     // ---------------------------------------------------------------- softmax rows
     if constexpr (KQ4 && VQ4) {
       if (args.app_flags != nullptr) {
@@ -1769,7 +1690,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
         // last visible key of this row, relative to the block
         const int rel_lim = (args.causal ? min(args.Sk - 1, pos) : args.Sk - 1) - kb;
         // O holds this segment's earlier blocks when j > j0
-        softmax_block<D, BF16, !C::kWide, C::kWide>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f,
+        softmax_block<D, BF16>(scol, ocol, need_mask, rel_lim, sl2, j > j0, f,
                                               l, nres, pmx);
         tmem_wait_st();
         tc_fence_before();
@@ -1827,45 +1748,6 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
                                      segs + sidx, ocol, active, f, l, nres, pmx, bar0, pseg,
                                      abort_flag, merge_flag);
         ++pseg;
-      }
-    }
-  } else if constexpr (C::kAnyQ4) {
-    if (C::is_dq_warp(warp)) {
-      // -------------------------------------------------------------- q4_0 dequant
-      // the dequant threads share out each raw tile's (key row, block) items and expand them
-      // into the 128B-swizzled f16/bf16 ring stage
-      const int u = C::dq_index(warp, lane);
-      const uint32_t mg = opaque_u32(BF16 ? 0x43004300u : 0x64006400u);
-      bool ok = true;
-      const int ntiles = static_cast<int>(2 * (t_end - t_begin));  // K and V of every step
-      int r = 0;  // raw q4_0 tiles consumed
-      for (int n = 0; n < ntiles; ++n) {
-        if (!((n & 1) ? VQ4 : KQ4)) continue;  // a dense tile: the producer's TMA fills it
-        const int rs = r % C::kRawStages;
-        const int s = n % C::kStages;
-        ok = mbar_wait(bar(kBarRawFull + rs), (r / C::kRawStages) & 1, abort_flag,
-                       &g_prefill_error);
-        if (ok && n >= C::kStages)
-          ok = mbar_wait(bar(kBarRingEmpty + s), ((n / C::kStages) - 1) & 1, abort_flag,
-                         &g_prefill_error);
-        if (!ok) break;
-        const uint8_t* raw = sgen + C::kOffRaw + rs * C::kRawBytes;
-        uint8_t* dst = sgen + C::kOffRing + s * C::kTileBytes;
-        // items (key row t, 32-element block blk) of the tile, rows fastest; unrolled so that
-        // the items' shared-memory loads overlap
-        constexpr int kItems = kBN * (D / 32);
-#pragma unroll
-        for (int k = 0; k < (kItems + C::kDqThreads - 1) / C::kDqThreads; ++k) {
-          const int it = u + k * C::kDqThreads;
-          if (kItems % C::kDqThreads == 0 || it < kItems)
-            dequant_item<D, BF16, C::kNibRow, C::kScaleRow, C::kRawNib>(raw, dst, it % kBN,
-                                                                        it / kBN, mg);
-        }
-        // generic-proxy writes must be visible to the tensor core's async proxy
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(bar(kBarRingFull + s));
-        mbar_arrive(bar(kBarRawEmpty + rs));
-        ++r;
       }
     }
   }
