@@ -104,6 +104,37 @@ def test_selfattn_b2_s512_h8_d64_full(fa):
     assert err < 5e-3
 
 
+@pytest.mark.parametrize("kv", ["dense", "q4_0"])
+def test_one_tile_launch_replayed_from_a_cuda_graph(fa, kv):
+    """The B2 S512 D64 self-attention (one query tile per CTA; dense K/V alternates S buffers)
+    captured once in a CUDA graph: replays with new query rows copied in must give the eager
+    result bit for bit."""
+    w = fa_inputs.WORKLOADS["selfattn_b2_s512_h8_d64_f16"]
+    q, k, v = fa_inputs.make_tensors(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.dtype, seed=17,
+                                     device="cuda")
+    if kv == "q4_0":
+        k, v = fa.fa_quantize_q4_0(k), fa.fa_quantize_q4_0(v)
+    qs, os_ = q.clone(), torch.empty_like(q)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fa.fa_fwd_ex(qs, k, v, os_, causal=True, q_pos_offset=0, stream=side)  # warm-up
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        fa.fa_fwd_ex(qs, k, v, os_, causal=True, q_pos_offset=0, stream=side)
+    for seed in (1, 2, 3):
+        qn = torch.randn(q.shape, generator=torch.Generator(device="cuda").manual_seed(seed),
+                         device="cuda").to(q.dtype)
+        qs.copy_(qn)
+        graph.replay()
+        torch.cuda.synchronize()
+        want = fa.fa_fwd_ex(qn, k, v, causal=True, q_pos_offset=0)
+        torch.cuda.synchronize()
+        assert torch.equal(os_, want), (kv, seed)
+    assert fa.fa_get_status() == fa.FA_OK
+
+
 def test_chunked_prefill_2k_full(fa):
     w = fa_inputs.WORKLOADS["prefill_gqa32x8_d128_sq2048_sk2048_f16"]
     run_case(fa, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, True, w.q_pos_offset, w.dtype, "dense",
