@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
             }
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        } else {
+        } else if constexpr (C::kAnyQ4) {  // a q4_0 side: raw stages exist
           const int s = r % C::kRawStages;
           if (r >= C::kRawStages) {
             if (lane == 0)
@@ -1290,7 +1290,7 @@ __global__ void __launch_bounds__(Cfg<D, KQ4, VQ4, true>::kThreads, 1)
             }
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        } else {
+        } else if constexpr (C::kAnyQ4) {  // a q4_0 side: raw stages exist
           const int s = r % C::kRawStages;
           if (r >= C::kRawStages) {
             if (lane == 0)
